@@ -1,0 +1,364 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for the selected-token logprob.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline / reference arm may load this library.  The
+ * product (the CUDA library under invariant_token_logprob_gb300/) never calls
+ * it and shares no code, header, table or helper with it.
+ *
+ * What it follows (pages cited by title and section):
+ *   [RLK]  "大模型强化学习后训练：如何通过 RL-Kernel 彻底消除训推 LogP 偏差"
+ *          (RL-Kernel blog), §一 (importance ratio, worked example),
+ *          §四 (five reduction classes; "Linear LogP" normalises over the whole
+ *          vocabulary; LogSumExp and its max-shifted stable form; blockwise
+ *          merge of per-block max m_j and exp-sum s_j).
+ *   [VLC]  "Finish RL Training Faster: Bitwise-Consistent, High-Performance,
+ *          Agent-Driven" (vLLM consistency blog summary), section
+ *          "训练-推理一致性的多维判定标准", paragraph "diff = 0 的数学定义"
+ *          (max / mean / std of |p_rollout - p_train| and the k3 KL r-1-log r).
+ *
+ * Readings where the pages are silent or garbled (each also listed in the
+ * design notes):
+ *   - The LSE formula itself is lost in the extraction of [RLK] §四; the
+ *     surviving sentence gives the stable form m + log sum exp(x_i - m), which
+ *     is what logprob_row() computes (two passes: max, then exp-sum).
+ *   - Temperature is not on the pages: z = (h . W_v) * inv_temp, one multiply by
+ *     the fp32 value of inv_temp, after the full dot product.
+ *   - Argmax ties go to the lowest vocabulary index.
+ *   - A target outside [0, V) is an ignored row: logp = 0.
+ *   - k3 uses r = exp(p_train - p_rollout) (probability ratio from the two
+ *     log-probabilities), computed as expm1(d) - d with d = a - b, a = train.
+ *   - std is the population standard deviation (divide by n_valid).
+ *
+ * Arithmetic: every floating-point step is in IEEE double.  bf16 -> double is
+ * exact, each bf16 x bf16 product is exact in double, the dot product is summed
+ * sequentially over k = 0..H-1.  Build without -ffast-math and with
+ * -ffp-contract=off so both host architectures give the same bits.
+ *
+ * ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake; the
+ * test suite builds each mutant to show that some pin fails for it.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+static double bf16_to_double(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* z[v] = (sum_k h[k] * W[v,k]) * inv_temp for v = 0..V-1 ([RLK] §四: the
+ * Linear LogP class scores the whole vocabulary).  hd holds h as doubles. */
+static void logits_row(const double *hd, const uint16_t *W, int64_t H,
+                       int64_t V, double inv_temp, double *z)
+{
+    for (int64_t v = 0; v < V; ++v) {
+        const uint16_t *w = W + v * H;
+        double acc = 0.0;
+#if ORACLE_MUTANT == 1
+        for (int64_t k = 0; k + 1 < H; ++k)      /* mutant: drops the last term */
+#else
+        for (int64_t k = 0; k < H; ++k)
+#endif
+            acc += hd[k] * bf16_to_double(w[k]);
+#if ORACLE_MUTANT == 2
+        z[v] = acc / inv_temp;                   /* mutant: divides by inv_temp */
+#else
+        z[v] = acc * inv_temp;
+#endif
+    }
+}
+
+typedef struct {
+    double logp, lse, zmax, ztgt, top2gap;
+    int64_t argmax;
+} row_result;
+
+/* One row: max, lowest-index argmax, two-pass LSE, selected-token logp. */
+static row_result logprob_row(const double *z, int64_t V, int32_t target)
+{
+    row_result r;
+    double m = z[0];
+    int64_t a = 0;
+    for (int64_t v = 1; v < V; ++v) {
+#if ORACLE_MUTANT == 3
+        if (z[v] >= m) { m = z[v]; a = v; }      /* mutant: highest index wins ties */
+#else
+        if (z[v] > m) { m = z[v]; a = v; }
+#endif
+    }
+    /* second pass: sum of exp(z - m); the stable form of [RLK] §四 */
+    double s = 0.0;
+    for (int64_t v = 0; v < V; ++v)
+        s += exp(z[v] - m);
+#if ORACLE_MUTANT == 4
+    double lse = log(s);                         /* mutant: forgets to add m back */
+#else
+    double lse = m + log(s);
+#endif
+    double second = -INFINITY;
+    for (int64_t v = 0; v < V; ++v)
+        if (v != a && z[v] > second) second = z[v];
+    r.zmax = m;
+    r.argmax = a;
+    r.lse = lse;
+    r.top2gap = m - second;                      /* +inf when V == 1 */
+    if (target >= 0 && (int64_t)target < V) {
+        r.ztgt = z[target];
+#if ORACLE_MUTANT == 5
+        r.logp = lse - z[target];                /* mutant: sign flipped */
+#else
+        r.logp = z[target] - lse;
+#endif
+    } else {
+        r.ztgt = 0.0;
+        r.logp = 0.0;                            /* ignored row */
+    }
+    return r;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Selected-token logprob for the rows listed in `rows` (or all T rows when
+ * rows == NULL; then n_rows must equal T).  h is [T,H] bf16 bits, W is [V,H]
+ * bf16 bits, both row-major.  Outputs are indexed by position in `rows`.
+ * Any output pointer may be NULL.  Returns 0, or -1 on bad arguments / memory.
+ */
+int oracle_logprob(const uint16_t *h, const uint16_t *W, const int32_t *targets,
+                   int64_t T, int64_t H, int64_t V, float inv_temp,
+                   const int64_t *rows, int64_t n_rows,
+                   double *out_logp, double *out_lse, int64_t *out_argmax,
+                   double *out_top2gap, double *out_ztgt, double *out_zmax)
+{
+    if (!h || !W || !targets || T < 0 || H <= 0 || V <= 0 || n_rows < 0)
+        return -1;
+    if (!rows && n_rows != T)
+        return -1;
+    int bad = 0;
+    const double it = (double)inv_temp;
+#pragma omp parallel
+    {
+        double *z = (double *)malloc((size_t)V * sizeof(double));
+        double *hd = (double *)malloc((size_t)H * sizeof(double));
+        if (!z || !hd) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_rows; ++i) {
+            if (!z || !hd) continue;
+            int64_t t = rows ? rows[i] : i;
+            if (t < 0 || t >= T) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            for (int64_t k = 0; k < H; ++k)
+                hd[k] = bf16_to_double(h[t * H + k]);
+            logits_row(hd, W, H, V, it, z);
+            row_result r = logprob_row(z, V, targets[t]);
+            if (out_logp) out_logp[i] = r.logp;
+            if (out_lse) out_lse[i] = r.lse;
+            if (out_argmax) out_argmax[i] = r.argmax;
+            if (out_top2gap) out_top2gap[i] = r.top2gap;
+            if (out_ztgt) out_ztgt[i] = r.ztgt;
+            if (out_zmax) out_zmax[i] = r.zmax;
+        }
+        free(z);
+        free(hd);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Per-block statistics of [RLK] §四 ("each block keeps a local max m_j and a
+ * local exp-sum s_j"): the vocabulary is cut into consecutive blocks of `bn`
+ * columns; block j covers columns [j*bn, min((j+1)*bn, V)).  For each listed
+ * row and block: m = max z, a = lowest index attaining m, s = sum exp(z - m)
+ * in ascending column order, zt = z[target] if the target lies in the block
+ * else 0.  Outputs are [n_rows][n_blocks] with n_blocks = ceil(V / bn).
+ */
+int oracle_block_stats(const uint16_t *h, const uint16_t *W, const int32_t *targets,
+                       int64_t T, int64_t H, int64_t V, float inv_temp, int64_t bn,
+                       const int64_t *rows, int64_t n_rows,
+                       double *out_m, double *out_s, int64_t *out_a, double *out_zt)
+{
+    if (!h || !W || !targets || T < 0 || H <= 0 || V <= 0 || bn <= 0 || n_rows < 0)
+        return -1;
+    if (!rows && n_rows != T)
+        return -1;
+    const int64_t nb = (V + bn - 1) / bn;
+    const double it = (double)inv_temp;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *z = (double *)malloc((size_t)V * sizeof(double));
+        double *hd = (double *)malloc((size_t)H * sizeof(double));
+        if (!z || !hd) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_rows; ++i) {
+            if (!z || !hd) continue;
+            int64_t t = rows ? rows[i] : i;
+            if (t < 0 || t >= T) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            for (int64_t k = 0; k < H; ++k)
+                hd[k] = bf16_to_double(h[t * H + k]);
+            logits_row(hd, W, H, V, it, z);
+            for (int64_t j = 0; j < nb; ++j) {
+                int64_t lo = j * bn, hi = lo + bn < V ? lo + bn : V;
+                double m = z[lo];
+                int64_t a = lo;
+                for (int64_t v = lo + 1; v < hi; ++v)
+                    if (z[v] > m) { m = z[v]; a = v; }
+                double s = 0.0;
+                for (int64_t v = lo; v < hi; ++v)
+                    s += exp(z[v] - m);
+                int32_t tg = targets[t];
+                double zt = (tg >= lo && tg < hi) ? z[tg] : 0.0;
+                if (out_m) out_m[i * nb + j] = m;
+                if (out_s) out_s[i * nb + j] = s;
+                if (out_a) out_a[i * nb + j] = a;
+                if (out_zt) out_zt[i * nb + j] = zt;
+            }
+        }
+        free(z);
+        free(hd);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Merge of per-block statistics ([RLK] §四 blockwise merge; §七 LogP: local
+ * statistics merged over vocabulary tiles).  The exact-arithmetic definition:
+ * M = max_j m_j, A = lowest a_j among blocks with m_j == M,
+ * S = sum_j s_j * exp(m_j - M), LSE = M + log S; logp = zt - LSE where zt is
+ * the target entry of the block holding the target.  Inputs are fp32 (the
+ * precision the partials are stored in), promoted to double; the sum runs over
+ * blocks in ascending order.  Blocks with m_j = -inf contribute nothing.
+ * Layout [n_rows][n_blocks]; targets are per row; bn is the block width used
+ * to find the target's block.  Returns 0 or -1.
+ */
+int oracle_merge_blocks(const float *m, const float *s, const int32_t *a,
+                        const float *zt, const int32_t *targets,
+                        int64_t n_rows, int64_t n_blocks, int64_t V, int64_t bn,
+                        double *out_lse, double *out_logp, int64_t *out_argmax)
+{
+    if (!m || !s || !a || n_rows < 0 || n_blocks <= 0 || V <= 0 || bn <= 0)
+        return -1;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const float *mr = m + r * n_blocks, *sr = s + r * n_blocks;
+        const int32_t *ar = a + r * n_blocks;
+        double M = -INFINITY;
+        int64_t A = INT64_MAX;
+        for (int64_t j = 0; j < n_blocks; ++j) {
+            double mj = (double)mr[j];
+            if (mj > M) { M = mj; A = ar[j]; }
+            else if (mj == M && ar[j] < A) A = ar[j];
+        }
+        double S = 0.0;
+        for (int64_t j = 0; j < n_blocks; ++j) {
+            double mj = (double)mr[j];
+            if (mj == -INFINITY) continue;
+            S += (double)sr[j] * exp(mj - M);
+        }
+        double lse = M + log(S);
+        if (out_lse) out_lse[r] = lse;
+        if (out_argmax) out_argmax[r] = A;
+        if (out_logp) {
+            double lp = 0.0;
+            if (targets && zt) {
+                int32_t tg = targets[r];
+                if (tg >= 0 && (int64_t)tg < V)
+                    lp = (double)zt[r * n_blocks + tg / bn] - lse;
+            }
+            out_logp[r] = lp;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Acceptance statistics of [VLC] "diff = 0 的数学定义" over valid tokens
+ * (mask == NULL: all valid; else mask[i] != 0 is valid).  a = train logp,
+ * b = rollout logp, d = a - b in double.
+ *   out[0] max |d|          out[1] mean |d|        out[2] population std of |d|
+ *   out[3] mean k3 = expm1(d) - d                  out[4] sum d
+ *   out[5] n_valid          out[6] number of valid i whose fp32 bit patterns differ
+ *   out[7] lowest valid index with differing bits, or -1
+ * With n_valid == 0 every statistic is 0 and out[7] = -1.  Returns 0 or -1.
+ */
+int oracle_consistency_stats(const float *a, const float *b, const int8_t *mask,
+                             int64_t n, double *out)
+{
+    if (!out || n < 0 || (n > 0 && (!a || !b)))
+        return -1;
+    double nv = 0.0, mx = 0.0, sabs = 0.0, sd = 0.0, sk3 = 0.0, nmis = 0.0;
+    int64_t first = -1;
+    for (int64_t i = 0; i < n; ++i) {
+        if (mask && mask[i] == 0) continue;
+#if ORACLE_MUTANT == 6
+        double d = (double)b[i] - (double)a[i];  /* mutant: direction swapped */
+#else
+        double d = (double)a[i] - (double)b[i];
+#endif
+        double ad = fabs(d);
+        nv += 1.0;
+        if (ad > mx) mx = ad;
+        sabs += ad;
+        sd += d;
+        sk3 += expm1(d) - d;
+        uint32_t ua, ub;
+        memcpy(&ua, &a[i], 4);
+        memcpy(&ub, &b[i], 4);
+        if (ua != ub) {
+            nmis += 1.0;
+            if (first < 0) first = i;
+        }
+    }
+    double mean = nv > 0 ? sabs / nv : 0.0;
+    double ss = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (mask && mask[i] == 0) continue;
+        double ad = fabs((double)a[i] - (double)b[i]);
+        ss += (ad - mean) * (ad - mean);
+    }
+#if ORACLE_MUTANT == 7
+    double var = nv > 1 ? ss / (nv - 1.0) : 0.0; /* mutant: sample variance */
+#else
+    double var = nv > 0 ? ss / nv : 0.0;
+#endif
+    out[0] = mx;
+    out[1] = mean;
+    out[2] = sqrt(var);
+    out[3] = nv > 0 ? sk3 / nv : 0.0;
+    out[4] = sd;
+    out[5] = nv;
+    out[6] = nmis;
+    out[7] = (double)first;
+    return 0;
+}

@@ -1,0 +1,326 @@
+"""Pins for the fp64 CPU oracle: each check ties it to something other than
+itself -- a closed form, an invariance of the mathematics, an exact brute force
+in arbitrary precision, a library routine (scipy) on an independent code path,
+or the pages' own worked example (tests/golden/).
+
+Every pin is a function of the loaded oracle library so that
+``test_pins_catch_planted_mistakes`` can run the same pins against oracle builds
+with a deliberate mistake planted (ORACLE_MUTANT in oracle.c) and show that each
+mistake fails at least one pin.
+"""
+import json
+import math
+import os
+
+import mpmath
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float -> bf16 bits by round-to-nearest-even (inputs here are bf16-exact)."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    back = (r.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(back, f), "test input is not bf16-exact"
+    return r
+
+
+def _bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------- pins
+
+def pin_zero_weights(lib):
+    """W = 0: every logit is 0, so LSE = ln V, logp = -ln V, argmax = 0 (lowest
+    index among V-way tie), top-2 gap 0."""
+    for V in (1, 7, 1024, 151936):
+        H, T = 16, 3
+        rng = np.random.default_rng(V)
+        h = _bf16_bits(rng.integers(-3, 4, size=(T, H)).astype(np.float32))
+        W = np.zeros((V, H), dtype=np.uint16)
+        tg = np.array([0, V - 1, V // 2], dtype=np.int32)
+        r = oracle.logprob(h, W, tg, 1.0, lib=lib)
+        lnV = float(mpmath.log(V))
+        assert np.allclose(r["lse"], lnV, rtol=0, atol=1e-12 * max(1.0, lnV))
+        assert np.allclose(r["logp"], -lnV, rtol=0, atol=1e-12 * max(1.0, lnV))
+        assert np.all(r["argmax"] == 0)
+        if V > 1:
+            assert np.all(r["top2gap"] == 0.0)
+
+
+def pin_one_hot_dominant(lib):
+    """h = c e_k, W[v*,k] = b, all else 0: z_{v*} = b c inv_temp, other z = 0.
+    logp(v*) = -log1p((V-1) exp(-z*)), logp(other) = -z* - log1p(...).
+    Uses the last hidden column k = H-1 in one case, and inv_temp != 1."""
+    cases = [(64, 1000, 5, 63, 2.0, 4.0, 1.0), (32, 4096, 4095, 31, 1.5, 3.0, 2.0),
+             (16, 77, 0, 0, -2.0, 4.0, 0.5)]
+    for H, V, vstar, k, c, b, it in cases:
+        h = np.zeros((2, H), np.float32)
+        h[:, k] = c
+        W = np.zeros((V, H), np.float32)
+        W[vstar, k] = b
+        other = (vstar + 1) % V
+        tg = np.array([vstar, other], np.int32)
+        r = oracle.logprob(_bf16_bits(h), _bf16_bits(W), tg, it, lib=lib)
+        zs = mpmath.mpf(b) * c * it
+        tail = mpmath.log1p((V - 1) * mpmath.exp(-zs))
+        exp_logp = [float(-tail), float(-zs - tail)]
+        exp_lse = float(zs + tail)
+        assert np.allclose(r["logp"], exp_logp, rtol=1e-13, atol=1e-13), (r["logp"], exp_logp)
+        assert np.allclose(r["lse"], exp_lse, rtol=1e-13, atol=1e-13)
+        if zs > 0:
+            assert np.all(r["argmax"] == vstar)
+        else:
+            assert np.all(r["argmax"] == (0 if vstar != 0 else 1))
+
+
+def pin_shift_invariance(lib):
+    """Append a hidden column equal to 1 and a weight column equal to c (bf16-exact):
+    every logit moves by c, so LSE moves by c and logp is unchanged."""
+    rng = np.random.default_rng(7)
+    T, H, V = 4, 48, 777
+    h = rng.standard_normal((T, H)).astype(np.float32)
+    W = (0.05 * rng.standard_normal((V, H))).astype(np.float32)
+    hb = _bits_to_f64(_bf16_bits_round(h)).astype(np.float32)
+    Wb = _bits_to_f64(_bf16_bits_round(W)).astype(np.float32)
+    tg = rng.integers(0, V, T).astype(np.int32)
+    base = oracle.logprob(_bf16_bits(hb), _bf16_bits(Wb), tg, 1.0, lib=lib)
+    for c in (3.0, -2.5, 0.125):
+        h2 = np.concatenate([hb, np.ones((T, 1), np.float32)], 1)
+        W2 = np.concatenate([Wb, np.full((V, 1), c, np.float32)], 1)
+        s = oracle.logprob(_bf16_bits(h2), _bf16_bits(W2), tg, 1.0, lib=lib)
+        assert np.allclose(s["lse"] - base["lse"], c, rtol=0, atol=1e-12)
+        assert np.allclose(s["logp"], base["logp"], rtol=0, atol=1e-12)
+        assert np.array_equal(s["argmax"], base["argmax"])
+
+
+def pin_temperature(lib):
+    """inv_temp = 2 is the same as doubling W (both exact), bit for bit in fp64;
+    inv_temp = 0.5 the same as halving W."""
+    rng = np.random.default_rng(11)
+    T, H, V = 3, 40, 500
+    h = _bf16_bits_round(rng.standard_normal((T, H)).astype(np.float32))
+    Wf = _bits_to_f64(_bf16_bits_round((0.05 * rng.standard_normal((V, H))).astype(np.float32)))
+    tg = rng.integers(0, V, T).astype(np.int32)
+    for it, scale in ((2.0, 2.0), (0.5, 0.5)):
+        a = oracle.logprob(h, _bf16_bits(Wf.astype(np.float32)), tg, it, lib=lib)
+        b = oracle.logprob(h, _bf16_bits((Wf * scale).astype(np.float32)), tg, 1.0, lib=lib)
+        for k in ("logp", "lse", "argmax", "zmax"):
+            assert np.array_equal(a[k], b[k]), k
+
+
+def pin_brute_force_exact(lib):
+    """Small-integer bf16 inputs: logits are exact integers (Python ints), LSE by
+    mpmath at 40 digits, argmax the lowest index of the exact maximum."""
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(3)
+    for trial in range(6):
+        T, H, V = 4, int(rng.integers(1, 17)), int(rng.integers(1, 33))
+        hi = rng.integers(-4, 5, size=(T, H))
+        Wi = rng.integers(-3, 4, size=(V, H))
+        if V > 3:
+            Wi[V - 1] = Wi[1]  # exact duplicate row: forces ties in some rows
+        it = (1.0, 0.5, 2.0)[trial % 3]
+        tg = rng.integers(-1, V, size=T).astype(np.int32)
+        r = oracle.logprob(_bf16_bits(hi.astype(np.float32)), _bf16_bits(Wi.astype(np.float32)),
+                           tg, it, lib=lib)
+        for t in range(T):
+            z = [int(sum(int(hi[t, k]) * int(Wi[v, k]) for k in range(H))) for v in range(V)]
+            zm = [mpmath.mpf(x) * mpmath.mpf(it) for x in z]
+            lse = mpmath.log(mpmath.fsum(mpmath.exp(x) for x in zm))
+            amax = z.index(max(z))
+            assert abs(r["lse"][t] - float(lse)) <= 1e-13 * max(1.0, abs(float(lse)))
+            assert r["argmax"][t] == amax
+            lp = float(zm[tg[t]] - lse) if tg[t] >= 0 else 0.0
+            assert abs(r["logp"][t] - lp) <= 1e-13 * max(1.0, abs(lp))
+            srt = sorted(zm, reverse=True)
+            gap = float(srt[0] - srt[1]) if V > 1 else math.inf
+            assert r["top2gap"][t] == gap
+
+
+def pin_scipy_logsumexp(lib):
+    """Independent code path: fp64 logits by numpy/BLAS matmul, LSE and
+    log-softmax by scipy.special; agreement to 1e-11."""
+    rng = np.random.default_rng(5)
+    T, H, V = 6, 96, 3001
+    h = _bf16_bits_round(rng.standard_normal((T, H)).astype(np.float32))
+    W = _bf16_bits_round((0.03 * rng.standard_normal((V, H))).astype(np.float32))
+    it = 1.0 / 0.7
+    tg = rng.integers(0, V, T).astype(np.int32)
+    r = oracle.logprob(h, W, tg, it, lib=lib)
+    z = (_bits_to_f64(h) @ _bits_to_f64(W).T) * float(np.float32(it))
+    lse = scipy.special.logsumexp(z, axis=1)
+    ls = scipy.special.log_softmax(z, axis=1)
+    assert np.allclose(r["lse"], lse, rtol=0, atol=1e-11)
+    assert np.allclose(r["logp"], ls[np.arange(T), tg], rtol=0, atol=1e-11)
+    assert np.array_equal(r["argmax"], np.argmax(z, axis=1))
+
+
+def pin_ignored_targets(lib):
+    """A target outside [0, V) is an ignored row: logp = 0, LSE still computed."""
+    rng = np.random.default_rng(9)
+    T, H, V = 4, 8, 50
+    h = _bf16_bits_round(rng.standard_normal((T, H)).astype(np.float32))
+    W = _bf16_bits_round(rng.standard_normal((V, H)).astype(np.float32))
+    tg = np.array([-1, V, -100, 3], np.int32)
+    r = oracle.logprob(h, W, tg, 1.0, lib=lib)
+    assert np.all(r["logp"][:3] == 0.0)
+    assert r["logp"][3] < 0.0
+    z = _bits_to_f64(h) @ _bits_to_f64(W).T
+    assert np.allclose(r["lse"], scipy.special.logsumexp(z, axis=1), atol=1e-11)
+
+
+def pin_block_stats_and_merge(lib):
+    """Per-block (m, s, a, zt) of the vocabulary against numpy on independently
+    computed logits; the fp64 merge of those blocks reproduces the whole-vocab
+    LSE / argmax / logp (the blockwise merge of the RL-Kernel blog, §四)."""
+    rng = np.random.default_rng(13)
+    T, H, V, bn = 5, 64, 1000, 128
+    h = _bf16_bits_round(rng.standard_normal((T, H)).astype(np.float32))
+    W = _bf16_bits_round((0.05 * rng.standard_normal((V, H))).astype(np.float32))
+    tg = rng.integers(0, V, T).astype(np.int32)
+    bs = oracle.block_stats(h, W, tg, bn, 1.0, lib=lib)
+    z = _bits_to_f64(h) @ _bits_to_f64(W).T
+    nb = (V + bn - 1) // bn
+    assert bs["m"].shape == (T, nb)
+    for j in range(nb):
+        zz = z[:, j * bn:min(V, (j + 1) * bn)]
+        assert np.allclose(bs["m"][:, j], zz.max(1), atol=1e-12)
+        assert np.array_equal(bs["a"][:, j], j * bn + zz.argmax(1))
+        assert np.allclose(bs["s"][:, j], np.exp(zz - zz.max(1, keepdims=True)).sum(1), rtol=1e-12)
+        inb = (tg >= j * bn) & (tg < (j + 1) * bn)
+        assert np.allclose(bs["zt"][inb, j], z[inb, tg[inb]], atol=1e-12)
+        assert np.all(bs["zt"][~inb, j] == 0.0)
+    full = oracle.logprob(h, W, tg, 1.0, lib=lib)
+    mg = oracle.merge_blocks(bs["m"].astype(np.float32), bs["s"].astype(np.float32),
+                             bs["a"].astype(np.int32), bs["zt"].astype(np.float32), tg, V, bn,
+                             lib=lib)
+    # fp32 storage of the partials costs ~1e-7 relative
+    assert np.allclose(mg["lse"], full["lse"], rtol=2e-7, atol=2e-7)
+    assert np.allclose(mg["logp"], full["logp"], rtol=0, atol=1e-6)
+    assert np.array_equal(mg["argmax"], full["argmax"])
+    # exact case: four equal blocks with m = 0, s = 1 -> LSE = ln 4, argmax = lowest a
+    m4 = np.zeros((1, 4), np.float32)
+    s4 = np.ones((1, 4), np.float32)
+    a4 = np.array([[30, 10, 20, 40]], np.int32)
+    e = oracle.merge_blocks(m4, s4, a4, None, None, 64, 16, lib=lib)
+    assert abs(e["lse"][0] - math.log(4.0)) < 1e-15 and e["argmax"][0] == 10
+    # a block at -inf (e.g. fully masked) contributes nothing
+    mi = np.array([[1.0, -np.inf]], np.float32)
+    si = np.array([[2.0, 0.0]], np.float32)
+    ai = np.array([[3, 0]], np.int32)
+    e = oracle.merge_blocks(mi, si, ai, None, None, 64, 32, lib=lib)
+    assert abs(e["lse"][0] - (1.0 + math.log(2.0))) < 1e-15 and e["argmax"][0] == 3
+
+
+def pin_worked_example(lib):
+    """The pages' worked example (tests/golden/worked_example.json): 200 tokens,
+    rollout -2.300, train -2.308: per-token ratio ~0.992, cumulative log-ratio
+    1.6, sequence ratio ~0.20; max = mean |gap| = 0.008, std 0."""
+    g = json.load(open(os.path.join(GOLDEN, "worked_example.json")))
+    n = g["n_tokens"]
+    a = np.full(n, g["train_logp"], np.float32)
+    b = np.full(n, g["rollout_logp"], np.float32)
+    st = oracle.consistency_stats(a, b, lib=lib)
+    gap32 = float(np.float64(np.float32(g["train_logp"])) - np.float64(np.float32(g["rollout_logp"])))
+    assert abs(st[0] - g["per_token_gap"]) < 1e-6 and abs(st[1] - g["per_token_gap"]) < 1e-6
+    assert st[0] == abs(gap32) and st[1] == pytest.approx(abs(gap32), rel=1e-15)
+    assert st[2] == pytest.approx(0.0, abs=1e-15)
+    assert st[4] == pytest.approx(-g["cumulative_log_gap_printed"], abs=1e-4)
+    assert round(math.exp(gap32), g["per_token_ratio_printed_decimals"]) == g["per_token_ratio_printed"]
+    assert round(math.exp(st[4]), g["sequence_ratio_printed_decimals"]) == g["sequence_ratio_printed"]
+    lo, hi = g["clip_interval_printed"]
+    assert not (lo <= math.exp(st[4]) <= hi)
+    assert st[5] == n and st[6] == n and st[7] == 0
+    # k3 = r - 1 - log r with log r = gap: closed form by mpmath
+    k3 = float(mpmath.expm1(mpmath.mpf(gap32)) - mpmath.mpf(gap32))
+    assert st[3] == pytest.approx(k3, rel=1e-12)
+
+
+def pin_stats_closed_forms(lib):
+    """Population std, masking, bit-mismatch counting, empty input, identity."""
+    b = np.array([0.0, 1.0, -2.0, 5.0, 7.0], np.float32)
+    a = b + np.array([1.0, -2.0, 3.0, 0.0, 100.0], np.float32)
+    mask = np.array([1, 1, 1, 1, 0], np.int8)
+    st = oracle.consistency_stats(a, b, mask, lib=lib)
+    # valid |d| = 1, 2, 3, 0: mean 1.5, population var 1.25
+    assert st[0] == 3.0 and st[1] == 1.5
+    assert st[2] == pytest.approx(math.sqrt(1.25), rel=1e-15)
+    assert st[4] == 2.0 and st[5] == 4 and st[6] == 3 and st[7] == 0
+    k3 = sum(float(mpmath.expm1(d) - d) for d in (1.0, -2.0, 3.0, 0.0)) / 4
+    assert st[3] == pytest.approx(k3, rel=1e-13)
+    # +0.0 vs -0.0: equal values, different bits
+    st = oracle.consistency_stats(np.array([1.0, 0.0], np.float32),
+                                  np.array([1.0, -0.0], np.float32), lib=lib)
+    assert st[0] == 0.0 and st[6] == 1 and st[7] == 1
+    # identical inputs: every statistic is exactly 0 (the pages' diff = 0)
+    x = np.random.default_rng(1).standard_normal(1000).astype(np.float32)
+    st = oracle.consistency_stats(x, x.copy(), lib=lib)
+    assert np.all(st[[0, 1, 2, 3, 4, 6]] == 0.0) and st[5] == 1000 and st[7] == -1
+    # nothing valid
+    st = oracle.consistency_stats(x, x + 1, np.zeros(1000, np.int8), lib=lib)
+    assert np.all(st[:7] == 0.0) and st[7] == -1
+    # small gaps: k3 ~ d^2 / 2 with no cancellation loss
+    d = np.float32(1e-6)
+    st = oracle.consistency_stats(np.array([d], np.float32), np.array([0.0], np.float32), lib=lib)
+    assert st[3] == pytest.approx(float(mpmath.expm1(mpmath.mpf(float(d))) - float(d)), rel=1e-9)
+
+
+def _bf16_bits_round(x: np.ndarray) -> np.ndarray:
+    """Round arbitrary fp32 to bf16 bits (RNE)."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+PINS = [pin_zero_weights, pin_one_hot_dominant, pin_shift_invariance, pin_temperature,
+        pin_brute_force_exact, pin_scipy_logsumexp, pin_ignored_targets,
+        pin_block_stats_and_merge, pin_worked_example, pin_stats_closed_forms]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_oracle_pin(pin, olib):
+    pin(olib)
+
+
+def test_tie_rows_of_tiny_input(olib):
+    """The tiny workload's forced ties resolve to the lower vocabulary index."""
+    import torch
+    from invariant_token_logprob_gb300.inputs import tiny_inputs
+    d = tiny_inputs(seed=0)
+    rows = torch.cat([d["dup_src"], d["dup_dst"]]).numpy()
+    r = oracle.logprob(d["h"], d["W"], d["targets"], 1.0, rows=rows, lib=olib)
+    exp = np.concatenate([d["expected_tie_argmax"].numpy()] * 2)
+    assert np.array_equal(r["argmax"], exp)
+    assert np.all(r["top2gap"] == 0.0)
+    # duplicated hidden rows give identical results
+    n = len(rows) // 2
+    for k in ("logp", "lse", "argmax"):
+        if k == "logp":
+            continue  # targets differ between the copies
+        assert np.array_equal(r[k][:n], r[k][n:])
+
+
+def test_pins_catch_planted_mistakes(tmp_path):
+    """Each deliberate mistake of oracle.c (ORACLE_MUTANT 1..7: dropped term,
+    divided temperature, highest-index ties, LSE without the max, flipped logp
+    sign, swapped gap direction, sample variance) fails at least one pin."""
+    for mutant in range(1, 8):
+        path = str(tmp_path / f"liboracle_m{mutant}.so")
+        oracle.build(path, mutant=mutant)
+        lib = oracle.load(path)
+        failed = []
+        for pin in PINS:
+            try:
+                pin(lib)
+            except AssertionError:
+                failed.append(pin.__name__)
+        assert failed, f"mutant {mutant} passed every pin"
