@@ -1,0 +1,197 @@
+/*
+ * rlk.h -- C ABI of the batch-invariant selected-token logprob library for
+ * GB300 (sm_103a).
+ *
+ * What the library computes.  For hidden states h[T,H] and LM-head weights
+ * W[V,H] (bf16), per row t:
+ *     z[t,v]     = fp32( sum_k h[t,k] * W[v,k] ) * inv_temp      (fp32 accumulate)
+ *     lse[t]     = log sum_v exp(z[t,v])                          (whole vocabulary)
+ *     logp[t]    = z[t,target[t]] - lse[t]
+ *     argmax[t]  = lowest v attaining max_v z[t,v]
+ * This is the "Linear LogP" reduction of the RL-Kernel blog
+ * ("大模型强化学习后训练：如何通过 RL-Kernel 彻底消除训推 LogP 偏差"), §四: the
+ * selected-token logprob depends on every vocabulary score through the LSE,
+ * computed blockwise (per-block max m_j and exp-sum s_j, then merged).  The
+ * GEMM accumulates the full K dimension in one fixed order with no split-K
+ * (same blog, §六 table row "GEMM": one CTA owns an output tile and walks all
+ * of K in a fixed order), and the per-block statistics are merged in a fixed
+ * vocabulary-tile order (§七 "LogP").
+ *
+ * Numerical contract (kept by construction and checked by the tests): the bits
+ * of a row's logp, lse and argmax depend only on that row's h, on W, on its
+ * target, on V, H and inv_temp -- never on T, on the row's position in the
+ * batch, on how a sequence is chunked into calls (prefill / decode / packed
+ * training), on the CUDA stream, or on repetition.  ("Finish RL Training
+ * Faster: Bitwise-Consistent, High-Performance, Agent-Driven", section
+ * "训练-推理一致性的多维判定标准": kernel determinism, batch independence and
+ * phase consistency.)  Tile shape, K order and merge tree are compile-time
+ * constants; nothing is chosen from T.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device (or managed) addresses on the current
+ *     device; host pointers are ordinary host memory.  The caller owns every
+ *     buffer it passes; the library keeps no pointer after a call returns.
+ *   - Matrices are row-major and dense: h is [T][H], W is [V][H], both bf16
+ *     (IEEE binary16-brain, raw 16-bit patterns), K (=H) contiguous.
+ *   - h, W and the workspace must be 16-byte aligned and H must be a multiple
+ *     of 8 (rows must start on 16-byte boundaries for the tensor-memory-access
+ *     engine).  Other device pointers need their natural alignment.
+ *   - Argument errors are detected on the host and returned before anything is
+ *     launched; nothing is printed and the library never aborts the process.
+ *   - Compute entry points are asynchronous on `stream` (NULL = the legacy
+ *     default stream) and perform no host synchronisation, unless stated.
+ *   - Requires a compute-capability 10.3 device (GB300); otherwise
+ *     RLK_ERR_UNSUPPORTED_DEVICE.  There is no CPU fallback.
+ */
+#ifndef RLK_H
+#define RLK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* A cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *rlk_stream_t;
+
+typedef enum rlk_status {
+    RLK_OK = 0,
+    RLK_ERR_INVALID_ARG = 1,        /* bad size, null pointer, bad inv_temp, ...      */
+    RLK_ERR_ALIGNMENT = 2,          /* pointer not 16-byte aligned or H % 8 != 0      */
+    RLK_ERR_UNSUPPORTED_DEVICE = 3, /* no CUDA device, or not compute capability 10.3 */
+    RLK_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed              */
+    RLK_ERR_WORKSPACE = 5,          /* workspace too small / could not be obtained    */
+    RLK_ERR_TIMEOUT = 6             /* a device-side bounded wait ran out (reported by
+                                       rlk_check_device_error)                       */
+} rlk_status;
+
+/* One per-(row, vocabulary tile) partial, as written by rlk_logprob_partials:
+ * m = max of z over the tile's columns, s = sum of exp(z - m) over them,
+ * a = lowest column index (absolute vocabulary index) attaining m,
+ * zt = z[target] if the row's target lies in this tile, else 0.0f. */
+typedef struct rlk_partial {
+    float m;
+    float s;
+    int32_t a;
+    float zt;
+} rlk_partial;
+
+/* ABI version of this header (bumped on any incompatible change). */
+#define RLK_ABI_VERSION 1
+int rlk_abi_version(void);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *rlk_status_string(int status);
+
+/* Compile-time tile shape: rows per row tile and vocabulary columns per tile.
+ * The number of vocabulary tiles of a problem is ceil(V / rlk_vocab_tile()). */
+int rlk_row_tile(void);
+int rlk_vocab_tile(void);
+
+/* Bytes of workspace rlk_logprob_ws needs: T * ceil(V / rlk_vocab_tile()) *
+ * sizeof(rlk_partial).  Returns 0 for T <= 0 or V <= 0. */
+size_t rlk_logprob_workspace_size(int64_t T, int64_t V);
+
+/*
+ * Selected-token logprob, LSE and argmax for T rows.
+ *   hidden_bf16   device, [T][H] bf16, 16-byte aligned
+ *   weight_bf16   device, [V][H] bf16, 16-byte aligned
+ *   targets_i32   device, [T]; a target outside [0, V) marks an ignored row:
+ *                 its logp is written as 0.0f (lse and argmax are still written)
+ *   T >= 0 (T == 0: returns RLK_OK, launches nothing), 1 <= H, H % 8 == 0,
+ *   1 <= V <= 2^31 - 1, T * ceil(V / vocab_tile) representable in int64
+ *   inv_temp      finite and > 0; z = fp32 accumulator * inv_temp (one multiply)
+ *   out_logp_f32, out_lse_f32  device, [T] float
+ *   out_argmax_i32             device, [T] int32
+ * Workspace: a per-(device, stream) buffer kept by the library, grown with
+ * cudaMallocAsync on `stream` when a call needs more, released by
+ * rlk_shutdown().  Two calls that share a stream share that buffer in stream
+ * order, which is safe; use rlk_logprob_ws to supply your own workspace.
+ */
+rlk_status rlk_logprob(const void *hidden_bf16, const void *weight_bf16,
+                       const int32_t *targets_i32, int64_t T, int64_t H, int64_t V,
+                       float inv_temp, float *out_logp_f32, float *out_lse_f32,
+                       int32_t *out_argmax_i32, rlk_stream_t stream);
+
+/* Same as rlk_logprob with a caller-owned device workspace of at least
+ * rlk_logprob_workspace_size(T, V) bytes, 16-byte aligned (else
+ * RLK_ERR_WORKSPACE / RLK_ERR_ALIGNMENT).  Allocates nothing. */
+rlk_status rlk_logprob_ws(const void *hidden_bf16, const void *weight_bf16,
+                          const int32_t *targets_i32, int64_t T, int64_t H, int64_t V,
+                          float inv_temp, float *out_logp_f32, float *out_lse_f32,
+                          int32_t *out_argmax_i32, void *workspace, size_t workspace_bytes,
+                          rlk_stream_t stream);
+
+/*
+ * Phase 1 alone: the LM-head GEMM with its fused vocabulary-tile epilogue
+ * (per-block max / exp-sum of the RL-Kernel blog §四, taken per fixed tile).
+ * Writes partials[t * NVT + j] for every row t < T and tile j < NVT =
+ * ceil(V / rlk_vocab_tile()); logits are never written to memory.
+ *   partials  device, 16-byte aligned, partials_bytes >= rlk_logprob_workspace_size(T, V)
+ * Other arguments as rlk_logprob.
+ */
+rlk_status rlk_logprob_partials(const void *hidden_bf16, const void *weight_bf16,
+                                const int32_t *targets_i32, int64_t T, int64_t H, int64_t V,
+                                float inv_temp, rlk_partial *partials, size_t partials_bytes,
+                                rlk_stream_t stream);
+
+/*
+ * Phase 2 alone: merge each row's NVT = ceil(V / rlk_vocab_tile()) partials
+ * in a fixed tree (the fixed vocabulary-tile-order merge of the RL-Kernel
+ * blog, §七 "LogP").  Per row: lane l of one warp folds tiles l, l+32, l+64, ...
+ * in ascending order, then five butterfly steps (xor 16, 8, 4, 2, 1) combine
+ * lanes.  The combine of (m1,s1,a1) and (m2,s2,a2) keeps the larger m (the
+ * lower a on equal m) as M and forms S = s_win + s_lose * exp(m_lose - M); it
+ * is commutative bit for bit, so every lane ends with the same bits.
+ * lse = M + log S, argmax = A, logp = zt(target's tile) - lse (0.0f for an
+ * ignored row).
+ *   partials  device, [T][NVT] rlk_partial (as written by rlk_logprob_partials
+ *             or by any producer keeping the same meaning), 16-byte aligned
+ *   targets_i32, outputs: as rlk_logprob.  T >= 0, V >= 1.
+ */
+rlk_status rlk_lse_merge(const rlk_partial *partials, const int32_t *targets_i32,
+                         int64_t T, int64_t V, float *out_logp_f32, float *out_lse_f32,
+                         int32_t *out_argmax_i32, rlk_stream_t stream);
+
+/*
+ * Acceptance statistics between two logprob vectors ("Finish RL Training
+ * Faster ...", paragraph "diff = 0 的数学定义": max, mean and std of
+ * |p_rollout - p_train| and the k3 KL r - 1 - log r).  a = train logp,
+ * b = rollout logp, d = a - b (in double), r = exp(d).  Over valid positions
+ * (mask == NULL: all; else mask[i] != 0):
+ *   out[0] max |d|   out[1] mean |d|   out[2] population std of |d|
+ *   out[3] mean (expm1(d) - d)         out[4] sum d
+ *   out[5] number of valid positions   out[6] valid positions whose fp32 bit
+ *   patterns differ                    out[7] lowest such index, or -1
+ * All statistics are 0 (out[7] = -1) when nothing is valid.
+ *   logp_a, logp_b  device, [n] float;  mask  device [n] int8 or NULL
+ *   out             HOST, 8 doubles
+ * Deterministic (fixed blocking and fixed reduction order for a given n).
+ * SYNCHRONOUS: returns after the result has been copied to `out`.
+ */
+rlk_status rlk_consistency_stats(const float *logp_a, const float *logp_b,
+                                 const int8_t *mask, int64_t n, double *out,
+                                 rlk_stream_t stream);
+
+/*
+ * Every device-side wait in the library's kernels is bounded in time.  If one
+ * runs out, the kernel records it in a per-device error word, drains its own
+ * in-flight copies, releases its tensor memory and returns (its outputs are
+ * then unspecified).  This call synchronises `stream`, reads and clears the
+ * word of the current device and returns RLK_ERR_TIMEOUT if it was set,
+ * RLK_ERR_CUDA if the stream reported an error, else RLK_OK.
+ */
+rlk_status rlk_check_device_error(rlk_stream_t stream);
+
+/* Release the library's cached workspaces on every device it used (waits for
+ * them to be idle).  Safe to call more than once. */
+rlk_status rlk_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLK_H */

@@ -1,0 +1,231 @@
+"""Batch-invariant selected-token logprob for GB300 (sm_103a).
+
+Thin ctypes binding over the C ABI of ``librlk.so`` (declared in
+``include/rlk.h``).  Functions here only marshal torch tensors into pointers,
+sizes and the current CUDA stream; every step of the computation runs in the
+library's CUDA kernels.  There is no CPU fallback: if the library is missing or
+the device is not compute capability 10.3 the calls raise.
+
+The library is loaded on first use, so ``invariant_token_logprob_gb300.inputs``
+(synthetic data) can be imported without it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+__all__ = ["RlkError", "lib", "logprob", "logprob_ws", "logprob_partials", "lse_merge",
+           "consistency_stats", "workspace_size", "check_device_error", "vocab_tile", "row_tile",
+           "header_functions", "STAT_NAMES", "LIB_PATH", "HEADER_PATH"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "librlk.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "rlk.h")
+
+STAT_NAMES = ("max_abs", "mean_abs", "std_abs", "k3_mean", "sum_delta", "n_valid",
+              "n_bit_mismatch", "first_mismatch")
+
+_STATUS = {0: "RLK_OK", 1: "RLK_ERR_INVALID_ARG", 2: "RLK_ERR_ALIGNMENT",
+           3: "RLK_ERR_UNSUPPORTED_DEVICE", 4: "RLK_ERR_CUDA", 5: "RLK_ERR_WORKSPACE",
+           6: "RLK_ERR_TIMEOUT"}
+
+
+class RlkError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        msg = _lib.rlk_status_string(int(status)).decode() if _lib is not None else _STATUS.get(status)
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C-ABI library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` (no CPU fallback exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+        f32, st = ctypes.c_float, ctypes.c_int
+        L.rlk_abi_version.restype = ctypes.c_int
+        L.rlk_abi_version.argtypes = []
+        L.rlk_status_string.restype = ctypes.c_char_p
+        L.rlk_status_string.argtypes = [ctypes.c_int]
+        L.rlk_row_tile.restype = ctypes.c_int
+        L.rlk_row_tile.argtypes = []
+        L.rlk_vocab_tile.restype = ctypes.c_int
+        L.rlk_vocab_tile.argtypes = []
+        L.rlk_logprob_workspace_size.restype = sz
+        L.rlk_logprob_workspace_size.argtypes = [i64, i64]
+        L.rlk_logprob.restype = st
+        L.rlk_logprob.argtypes = [P, P, P, i64, i64, i64, f32, P, P, P, P]
+        L.rlk_logprob_ws.restype = st
+        L.rlk_logprob_ws.argtypes = [P, P, P, i64, i64, i64, f32, P, P, P, P, sz, P]
+        L.rlk_logprob_partials.restype = st
+        L.rlk_logprob_partials.argtypes = [P, P, P, i64, i64, i64, f32, P, sz, P]
+        L.rlk_lse_merge.restype = st
+        L.rlk_lse_merge.argtypes = [P, P, i64, i64, P, P, P, P]
+        L.rlk_consistency_stats.restype = st
+        L.rlk_consistency_stats.argtypes = [P, P, P, i64, P, P]
+        L.rlk_check_device_error.restype = st
+        L.rlk_check_device_error.argtypes = [P]
+        L.rlk_shutdown.restype = st
+        L.rlk_shutdown.argtypes = []
+        _lib = L
+    return _lib
+
+
+def header_functions(path: str = HEADER_PATH) -> list:
+    """Names of the functions include/rlk.h declares."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rlk_[a-z_0-9]+)\s*\(", text)))
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise RlkError(status, where)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, ndim=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device (no CPU path exists)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def row_tile() -> int:
+    return lib().rlk_row_tile()
+
+
+def vocab_tile() -> int:
+    return lib().rlk_vocab_tile()
+
+
+def workspace_size(T: int, V: int) -> int:
+    return lib().rlk_logprob_workspace_size(int(T), int(V))
+
+
+def _check_inputs(h, W, targets):
+    import torch
+    _need(h, torch.bfloat16, "h", 2)
+    _need(W, torch.bfloat16, "W", 2)
+    _need(targets, torch.int32, "targets", 1)
+    T, H = h.shape
+    V, H2 = W.shape
+    if H != H2 or targets.shape[0] != T:
+        raise ValueError("shape mismatch: h [T,H], W [V,H], targets [T]")
+    return T, H, V
+
+
+def _outputs(T, device, out):
+    import torch
+    if out is None:
+        return (torch.empty(T, dtype=torch.float32, device=device),
+                torch.empty(T, dtype=torch.float32, device=device),
+                torch.empty(T, dtype=torch.int32, device=device))
+    lp, lse, am = out
+    _need(lp, torch.float32, "out[0]", 1)
+    _need(lse, torch.float32, "out[1]", 1)
+    _need(am, torch.int32, "out[2]", 1)
+    return lp, lse, am
+
+
+def logprob(h, W, targets, inv_temp: float = 1.0, out=None, stream=None):
+    """rlk_logprob: returns (logp f32[T], lse f32[T], argmax i32[T]) on h's device."""
+    T, H, V = _check_inputs(h, W, targets)
+    lp, lse, am = _outputs(T, h.device, out)
+    _check(lib().rlk_logprob(_ptr(h), _ptr(W), _ptr(targets), T, H, V, ctypes.c_float(inv_temp),
+                             _ptr(lp), _ptr(lse), _ptr(am), _stream(stream)), "rlk_logprob")
+    return lp, lse, am
+
+
+def logprob_ws(h, W, targets, workspace, inv_temp: float = 1.0, out=None, stream=None):
+    """rlk_logprob_ws with a caller-owned uint8 CUDA workspace tensor."""
+    import torch
+    T, H, V = _check_inputs(h, W, targets)
+    _need(workspace, torch.uint8, "workspace", 1)
+    lp, lse, am = _outputs(T, h.device, out)
+    _check(lib().rlk_logprob_ws(_ptr(h), _ptr(W), _ptr(targets), T, H, V, ctypes.c_float(inv_temp),
+                                _ptr(lp), _ptr(lse), _ptr(am), _ptr(workspace),
+                                workspace.numel(), _stream(stream)), "rlk_logprob_ws")
+    return lp, lse, am
+
+
+def logprob_partials(h, W, targets, inv_temp: float = 1.0, out=None, stream=None):
+    """rlk_logprob_partials: returns a float32 tensor [T, NVT, 4] of {m, s, a-bits, zt}
+    (view column 2 as int32 for the argmax)."""
+    import torch
+    T, H, V = _check_inputs(h, W, targets)
+    nvt = (V + vocab_tile() - 1) // vocab_tile()
+    if out is None:
+        out = torch.empty((T, nvt, 4), dtype=torch.float32, device=h.device)
+    _need(out, torch.float32, "out")
+    _check(lib().rlk_logprob_partials(_ptr(h), _ptr(W), _ptr(targets), T, H, V,
+                                      ctypes.c_float(inv_temp), _ptr(out),
+                                      out.numel() * 4, _stream(stream)), "rlk_logprob_partials")
+    return out
+
+
+def lse_merge(partials, targets, V: int, out=None, stream=None):
+    """rlk_lse_merge over a [T, NVT, 4] float32 partial tensor."""
+    import torch
+    _need(partials, torch.float32, "partials", 3)
+    _need(targets, torch.int32, "targets", 1)
+    T = partials.shape[0]
+    nvt = (V + vocab_tile() - 1) // vocab_tile()
+    if partials.shape[1] != nvt or partials.shape[2] != 4 or targets.shape[0] != T:
+        raise ValueError("partials must be [T, ceil(V/vocab_tile), 4] and targets [T]")
+    lp, lse, am = _outputs(T, partials.device, out)
+    _check(lib().rlk_lse_merge(_ptr(partials), _ptr(targets), T, int(V), _ptr(lp), _ptr(lse),
+                               _ptr(am), _stream(stream)), "rlk_lse_merge")
+    return lp, lse, am
+
+
+def consistency_stats(a, b, mask=None, stream=None):
+    """rlk_consistency_stats (synchronous): a = train logp, b = rollout logp (f32 CUDA
+    tensors), optional int8 mask; returns a dict keyed by STAT_NAMES."""
+    import torch
+    _need(a, torch.float32, "a", 1)
+    _need(b, torch.float32, "b", 1)
+    if a.shape != b.shape:
+        raise ValueError("a and b must have the same shape")
+    mp = None
+    if mask is not None:
+        _need(mask, torch.int8, "mask", 1)
+        if mask.shape != a.shape:
+            raise ValueError("mask must match a")
+        mp = _ptr(mask)
+    out = (ctypes.c_double * 8)()
+    _check(lib().rlk_consistency_stats(_ptr(a), _ptr(b), mp, a.shape[0], out, _stream(stream)),
+           "rlk_consistency_stats")
+    return dict(zip(STAT_NAMES, list(out)))
+
+
+def check_device_error(stream=None):
+    """Raise RlkError(RLK_ERR_TIMEOUT) if a device-side bounded wait ran out."""
+    _check(lib().rlk_check_device_error(_stream(stream)), "rlk_check_device_error")

@@ -1,0 +1,324 @@
+// rlk_api.cu -- the C ABI declared in include/rlk.h: host-side argument
+// checks, tensor-map encoding, the per-(device, stream) workspace cache and
+// the two launches of the logprob path (fused GEMM/epilogue, then merge).
+// Nothing here computes on the host: every step of the path runs in the
+// library's kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "rlk.h"
+#include "rlk_internal.h"
+
+namespace {
+
+using rlk::kKBlock;
+using rlk::kRowTile;
+using rlk::kVocabTile;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int checked = 0;  // 0 unknown, 1 supported, -1 unsupported
+    int num_sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_tried = false;
+
+struct WsEntry {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, WsEntry> g_ws;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+rlk_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return RLK_OK;
+    if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ||
+        e == cudaErrorInvalidDevice)
+        return RLK_ERR_UNSUPPORTED_DEVICE;
+    return RLK_ERR_CUDA;
+}
+
+// Current device must be compute capability 10.3; returns its SM count.
+rlk_status current_device(int* dev_out, int* sms_out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return from_cuda(e) == RLK_ERR_CUDA ? RLK_ERR_UNSUPPORTED_DEVICE : from_cuda(e);
+    }
+    if (dev < 0 || dev >= kMaxDevices) return RLK_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& di = g_dev[dev];
+    if (di.checked == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return RLK_ERR_UNSUPPORTED_DEVICE;
+        }
+        di.checked = (major == 10 && minor == 3) ? 1 : -1;
+        di.num_sms = sms;
+    }
+    if (di.checked != 1) return RLK_ERR_UNSUPPORTED_DEVICE;
+    *dev_out = dev;
+    *sms_out = di.num_sms;
+    return RLK_OK;
+}
+
+EncodeTiledFn encode_fn() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode_tried) {
+        g_encode_tried = true;
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        else
+            cudaGetLastError();
+    }
+    return g_encode;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix, box {kKBlock, box_rows},
+// 128-byte swizzle, zero fill outside the matrix.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                    int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(kKBlock), cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int64_t num_vocab_tiles(int64_t V) { return (V + kVocabTile - 1) / kVocabTile; }
+
+// Shape / value checks shared by every logprob entry point (host only).
+rlk_status check_shape(int64_t T, int64_t H, int64_t V, float inv_temp) {
+    if (T < 0 || H < 1 || V < 1) return RLK_ERR_INVALID_ARG;
+    if (V > INT32_MAX || T > INT32_MAX || H > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    if (!(inv_temp > 0.0f) || !isfinite(inv_temp)) return RLK_ERR_INVALID_ARG;
+    const int64_t row_tiles = (T + kRowTile - 1) / kRowTile;
+    if (row_tiles * num_vocab_tiles(V) > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    return RLK_OK;
+}
+
+rlk_status check_operands(const void* h, const void* W, const int32_t* tg, int64_t H) {
+    if (!h || !W || !tg) return RLK_ERR_INVALID_ARG;
+    if ((H % 8) != 0 || !aligned16(h) || !aligned16(W) || !aligned4(tg)) return RLK_ERR_ALIGNMENT;
+    return RLK_OK;
+}
+
+rlk_status check_outputs(const float* lp, const float* lse, const int32_t* am) {
+    if (!lp || !lse || !am) return RLK_ERR_INVALID_ARG;
+    if (!aligned4(lp) || !aligned4(lse) || !aligned4(am)) return RLK_ERR_ALIGNMENT;
+    return RLK_OK;
+}
+
+rlk_status launch_partials(const void* h, const void* W, const int32_t* tg, int64_t T,
+                           int64_t H, int64_t V, float inv_temp, void* partials, int num_sms,
+                           cudaStream_t stream) {
+    CUtensorMap th, tw;
+    if (!encode_bf16_2d(&th, h, T, H, kRowTile) || !encode_bf16_2d(&tw, W, V, H, kVocabTile))
+        return RLK_ERR_CUDA;
+    return from_cuda(rlk::launch_lmhead_partials(&th, &tw, tg, partials, T, V, H, inv_temp,
+                                                 num_sms, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int rlk_abi_version(void) { return RLK_ABI_VERSION; }
+
+const char* rlk_status_string(int status) {
+    switch (status) {
+        case RLK_OK: return "RLK_OK";
+        case RLK_ERR_INVALID_ARG: return "RLK_ERR_INVALID_ARG: invalid argument";
+        case RLK_ERR_ALIGNMENT: return "RLK_ERR_ALIGNMENT: pointer not aligned or H % 8 != 0";
+        case RLK_ERR_UNSUPPORTED_DEVICE:
+            return "RLK_ERR_UNSUPPORTED_DEVICE: needs a compute capability 10.3 GPU";
+        case RLK_ERR_CUDA: return "RLK_ERR_CUDA: a CUDA call failed";
+        case RLK_ERR_WORKSPACE: return "RLK_ERR_WORKSPACE: workspace too small or unavailable";
+        case RLK_ERR_TIMEOUT: return "RLK_ERR_TIMEOUT: a device-side bounded wait ran out";
+        default: return "unknown rlk_status";
+    }
+}
+
+int rlk_row_tile(void) { return kRowTile; }
+int rlk_vocab_tile(void) { return kVocabTile; }
+
+size_t rlk_logprob_workspace_size(int64_t T, int64_t V) {
+    if (T <= 0 || V <= 0) return 0;
+    return size_t(T) * size_t(num_vocab_tiles(V)) * sizeof(rlk_partial);
+}
+
+rlk_status rlk_logprob_partials(const void* hidden_bf16, const void* weight_bf16,
+                                const int32_t* targets_i32, int64_t T, int64_t H, int64_t V,
+                                float inv_temp, rlk_partial* partials, size_t partials_bytes,
+                                rlk_stream_t stream) {
+    rlk_status st = check_shape(T, H, V, inv_temp);
+    if (st != RLK_OK) return st;
+    if (T == 0) return RLK_OK;
+    if ((st = check_operands(hidden_bf16, weight_bf16, targets_i32, H)) != RLK_OK) return st;
+    if (!partials) return RLK_ERR_INVALID_ARG;
+    if (!aligned16(partials)) return RLK_ERR_ALIGNMENT;
+    if (partials_bytes < rlk_logprob_workspace_size(T, V)) return RLK_ERR_WORKSPACE;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    return launch_partials(hidden_bf16, weight_bf16, targets_i32, T, H, V, inv_temp, partials,
+                           sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+rlk_status rlk_lse_merge(const rlk_partial* partials, const int32_t* targets_i32, int64_t T,
+                         int64_t V, float* out_logp_f32, float* out_lse_f32,
+                         int32_t* out_argmax_i32, rlk_stream_t stream) {
+    if (T < 0 || V < 1 || V > INT32_MAX || T > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    if (T == 0) return RLK_OK;
+    if (!partials || !targets_i32) return RLK_ERR_INVALID_ARG;
+    rlk_status st = check_outputs(out_logp_f32, out_lse_f32, out_argmax_i32);
+    if (st != RLK_OK) return st;
+    if (!aligned16(partials) || !aligned4(targets_i32)) return RLK_ERR_ALIGNMENT;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    return from_cuda(rlk::launch_lse_merge(partials, targets_i32, T, V, out_logp_f32, out_lse_f32,
+                                           out_argmax_i32, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rlk_status rlk_logprob_ws(const void* hidden_bf16, const void* weight_bf16,
+                          const int32_t* targets_i32, int64_t T, int64_t H, int64_t V,
+                          float inv_temp, float* out_logp_f32, float* out_lse_f32,
+                          int32_t* out_argmax_i32, void* workspace, size_t workspace_bytes,
+                          rlk_stream_t stream) {
+    rlk_status st = check_shape(T, H, V, inv_temp);
+    if (st != RLK_OK) return st;
+    if (T == 0) return RLK_OK;
+    if ((st = check_operands(hidden_bf16, weight_bf16, targets_i32, H)) != RLK_OK) return st;
+    if ((st = check_outputs(out_logp_f32, out_lse_f32, out_argmax_i32)) != RLK_OK) return st;
+    if (!workspace) return RLK_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return RLK_ERR_ALIGNMENT;
+    if (workspace_bytes < rlk_logprob_workspace_size(T, V)) return RLK_ERR_WORKSPACE;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = launch_partials(hidden_bf16, weight_bf16, targets_i32, T, H, V, inv_temp, workspace, sms,
+                         s);
+    if (st != RLK_OK) return st;
+    return from_cuda(rlk::launch_lse_merge(workspace, targets_i32, T, V, out_logp_f32,
+                                           out_lse_f32, out_argmax_i32, s));
+}
+
+rlk_status rlk_logprob(const void* hidden_bf16, const void* weight_bf16,
+                       const int32_t* targets_i32, int64_t T, int64_t H, int64_t V,
+                       float inv_temp, float* out_logp_f32, float* out_lse_f32,
+                       int32_t* out_argmax_i32, rlk_stream_t stream) {
+    rlk_status st = check_shape(T, H, V, inv_temp);
+    if (st != RLK_OK) return st;
+    if (T == 0) return RLK_OK;
+    if ((st = check_operands(hidden_bf16, weight_bf16, targets_i32, H)) != RLK_OK) return st;
+    if ((st = check_outputs(out_logp_f32, out_lse_f32, out_argmax_i32)) != RLK_OK) return st;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t need = rlk_logprob_workspace_size(T, V);
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        WsEntry& w = g_ws[std::make_pair(dev, s)];
+        if (w.bytes < need) {
+            if (w.ptr) {
+                if (cudaFreeAsync(w.ptr, s) != cudaSuccess) {
+                    cudaGetLastError();
+                    return RLK_ERR_WORKSPACE;
+                }
+                w.ptr = nullptr;
+                w.bytes = 0;
+            }
+            // grow geometrically so a sweep over T does not reallocate every call
+            size_t want = need + need / 4;
+            if (cudaMallocAsync(&w.ptr, want, s) != cudaSuccess) {
+                cudaGetLastError();
+                w.ptr = nullptr;
+                return RLK_ERR_WORKSPACE;
+            }
+            w.bytes = want;
+        }
+        ws = w.ptr;
+    }
+    st = launch_partials(hidden_bf16, weight_bf16, targets_i32, T, H, V, inv_temp, ws, sms, s);
+    if (st != RLK_OK) return st;
+    return from_cuda(rlk::launch_lse_merge(ws, targets_i32, T, V, out_logp_f32, out_lse_f32,
+                                           out_argmax_i32, s));
+}
+
+rlk_status rlk_consistency_stats(const float* logp_a, const float* logp_b, const int8_t* mask,
+                                 int64_t n, double* out, rlk_stream_t stream) {
+    if (!out || n < 0) return RLK_ERR_INVALID_ARG;
+    if (n == 0) {
+        for (int i = 0; i < 7; ++i) out[i] = 0.0;
+        out[7] = -1.0;
+        return RLK_OK;
+    }
+    if (!logp_a || !logp_b) return RLK_ERR_INVALID_ARG;
+    if (!aligned4(logp_a) || !aligned4(logp_b)) return RLK_ERR_ALIGNMENT;
+    int dev, sms;
+    rlk_status st = current_device(&dev, &sms);
+    if (st != RLK_OK) return st;
+    return from_cuda(rlk::run_consistency_stats(logp_a, logp_b, mask, n, out,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rlk_status rlk_check_device_error(rlk_stream_t stream) {
+    int dev, sms;
+    rlk_status st = current_device(&dev, &sms);
+    if (st != RLK_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return RLK_ERR_CUDA;
+    unsigned int word = 0;
+    if (rlk::lmhead_take_error(&word) != cudaSuccess) return RLK_ERR_CUDA;
+    return word ? RLK_ERR_TIMEOUT : RLK_OK;
+}
+
+rlk_status rlk_shutdown(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    rlk_status st = RLK_OK;
+    int prev = -1;
+    bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
+    for (auto& kv : g_ws) {
+        if (!kv.second.ptr) continue;
+        if (cudaSetDevice(kv.first.first) != cudaSuccess || cudaFree(kv.second.ptr) != cudaSuccess) {
+            cudaGetLastError();
+            st = RLK_ERR_CUDA;
+        }
+    }
+    g_ws.clear();
+    if (have_prev) cudaSetDevice(prev);
+    return st;
+}
+
+}  // extern "C"

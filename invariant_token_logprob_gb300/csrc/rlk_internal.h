@@ -1,0 +1,36 @@
+// rlk_internal.h -- launchers shared between the translation units of the
+// library (not part of the public C ABI; see include/rlk.h for that).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rlk {
+
+// Compile-time tile shape of the LM-head kernel.  The tile never depends on T.
+constexpr int kRowTile = 128;    // rows per tile  = UMMA M
+constexpr int kVocabTile = 256;  // columns per tile = UMMA N
+constexpr int kKBlock = 64;      // K elements per pipeline stage (one 128-B swizzle row)
+
+// Fused LM-head GEMM + vocabulary-tile epilogue.  Writes partials[T][NVT]
+// (16-byte records {m, s, a, zt}).  th / tw are 2-D tensor maps of h [T,H] and
+// W [V,H] with boxes {kKBlock, kRowTile} / {kKBlock, kVocabTile}, 128-B swizzle.
+cudaError_t launch_lmhead_partials(const CUtensorMap* th, const CUtensorMap* tw,
+                                   const int32_t* targets, void* partials, int64_t T, int64_t V,
+                                   int64_t H, float inv_temp, int num_sms, cudaStream_t stream);
+
+// Reads and clears the per-device error word of the LM-head kernel (bit 0: a
+// bounded wait ran out).  Synchronous on the current device.
+cudaError_t lmhead_take_error(unsigned int* out);
+
+// Fixed-tree merge of the partials into logp / lse / argmax.
+cudaError_t launch_lse_merge(const void* partials, const int32_t* targets, int64_t T, int64_t V,
+                             float* out_logp, float* out_lse, int32_t* out_argmax,
+                             cudaStream_t stream);
+
+// Consistency statistics; synchronous, result in host memory (8 doubles).
+cudaError_t run_consistency_stats(const float* a, const float* b, const int8_t* mask, int64_t n,
+                                  double* host_out, cudaStream_t stream);
+
+}  // namespace rlk

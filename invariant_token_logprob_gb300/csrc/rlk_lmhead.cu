@@ -1,0 +1,366 @@
+// rlk_lmhead.cu -- the LM-head GEMM on the 5th-generation tensor core with a
+// fused vocabulary-tile epilogue (sm_103a).
+//
+// What it computes (RL-Kernel blog "大模型强化学习后训练：如何通过 RL-Kernel
+// 彻底消除训推 LogP 偏差", §四 Linear LogP + blockwise LSE statistics; §六 table
+// row "GEMM": one CTA owns an output tile and accumulates the whole K dimension
+// in a fixed order, no split-K):
+//   for every (row tile m, vocabulary tile n) of the fixed 128 x 256 grid,
+//     acc[r, c] = sum_k h[r, k] W[c, k]          bf16 x bf16 -> fp32 in TMEM,
+//                                                k = 0, 16, 32, ... in order
+//     z = acc * inv_temp                          one fp32 multiply
+//     per row r: (m, s, a) over the tile's columns, built from 32-column chunks
+//       (chunk max, lowest argmax, sum exp(z - chunk max) in column order) folded
+//       left to right with lse_combine; zt = z[target] if the target is here.
+//   The record {m, s, a, zt} goes to partials[r][n]; logits never reach HBM.
+//
+// Why the bits cannot depend on T or on a row's batch position: the tile shape,
+// K order and epilogue order are compile-time constants; a row's accumulator is
+// produced by the same MMA instructions over the same K steps whichever tile
+// row (TMEM lane) it occupies, rows never mix, and which CTA processes a tile
+// only changes when it is done, not how.
+//
+// Structure: one persistent CTA per SM (grid = min(#tiles, #SMs)), 6 warps:
+//   warp 0      TMA producer: h and W k-blocks into a 4-stage smem ring
+//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=16) per stage;
+//               also allocates / frees the 512 TMEM columns
+//   warps 2..5  epilogue: TMEM -> registers -> partial record; one thread per
+//               row, warp w reads TMEM lanes 32*(w%4) .. +31
+// The accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue
+// of tile i overlaps the MMAs of tile i+1.  Every wait is bounded in time.
+#include <limits.h>
+
+#include "rlk_internal.h"
+#include "rlk_lse.cuh"
+#include "rlk_sm103.cuh"
+
+namespace rlk {
+namespace {
+
+constexpr int kBM = kRowTile;
+constexpr int kBN = kVocabTile;
+constexpr int kBK = kKBlock;
+constexpr int kUK = 16;  // K per tcgen05.mma kind::f16
+constexpr int kStages = 4;
+constexpr int kAccBufs = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
+constexpr int kBBytes = kBN * kBK * 2;  // 32 KiB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 192;
+constexpr int kBarriers = 2 * kStages + 2 * kAccBufs + 1;
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + size_t(kStages) * kStageBytes +
+                              kBarriers * 8 + 16;
+constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for teardown waits
+
+static_assert(kBK * 2 == 128, "one k-block is one 128-byte swizzle row");
+static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "stage tiles 1024-B aligned");
+static_assert(kAccBufs * kBN <= int(kTmemCols), "TMEM budget");
+
+__device__ unsigned int g_lmhead_error;
+
+struct Args {
+    const int32_t* targets;
+    float4* partials;
+    int64_t T;
+    int V;
+    int num_m;   // row tiles
+    int num_n;   // vocabulary tiles (NVT)
+    int num_kb;  // k-blocks
+    int band;    // row tiles per raster band (schedule only; never affects values)
+    int num_tiles;
+    float inv_temp;
+};
+
+// Raster: bands of `band` row tiles; inside a band, vocabulary tile outer and
+// row tile inner, so CTAs running together share one W tile through L2 and
+// the band's h rows stay L2-resident while W streams past once per band.
+__device__ __forceinline__ void tile_coords(const Args& p, int tile, int& m, int& n) {
+    const int band_tiles = p.band * p.num_n;
+    const int b = tile / band_tiles;
+    const int rem = tile - b * band_tiles;
+    const int rows = min(p.band, p.num_m - b * p.band);
+    n = rem / rows;
+    m = b * p.band + (rem - n * rows);
+}
+
+// Wait for phase `parity` of `bar`, giving up after kWaitLimitNs (then the
+// error word and the CTA's abort flag are set) or when another role of the
+// CTA has already given up.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++spins & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(&g_lmhead_error, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+// Teardown wait: bounded, ignores the abort flag.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kDrainLimitNs) {
+            atomicOr(&g_lmhead_error, 2u);
+            return;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    lmhead_partials_kernel(const __grid_constant__ CUtensorMap tmap_h,
+                           const __grid_constant__ CUtensorMap tmap_w, const Args p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t tiles_addr = raw_addr + pad;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBarriers);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    auto full_bar = [&](int s) { return smem_u32(bars + s); };
+    auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
+    auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * kStages + b); };
+    auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * kStages + kAccBufs + b); };
+    const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 2 * kAccBufs);
+    auto a_tile = [&](int s) { return tiles_addr + uint32_t(s) * kStageBytes; };
+    auto b_tile = [&](int s) { return tiles_addr + uint32_t(s) * kStageBytes + kABytes; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < kAccBufs; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_h);
+        tma_prefetch_desc(&tmap_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                int m, n;
+                tile_coords(p, tile, m, n);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+                    tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage), kb * kBK, m * kBM);
+                    tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), kb * kBK, n * kBN);
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let the copies this thread started land before the CTA exits.
+                const int first = issued > kStages ? issued - kStages : 0;
+                for (int i = first; i < issued; ++i)
+                    wait_drain(full_bar(i % kStages), uint32_t(i / kStages) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            uint32_t acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + acc * uint32_t(kBN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(full_bar(stage), phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage));
+                    const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage));
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUK; ++kk) {
+                        // advance the start address by kk * 32 bytes inside the swizzle row
+                        const uint64_t off = uint64_t((kk * kUK * 2) >> 4);
+                        umma_bf16(d_tmem, a_desc + off, b_desc + off, kIdesc,
+                                  (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(stage));  // frees the smem stage when these MMAs finish
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+                if (++acc == kAccBufs) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // No MMA may still be writing TMEM when it is freed.
+            umma_commit(drain_bar);
+            wait_drain(drain_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const int row_in_tile = q * 32 + lane;
+        const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16);
+        const float inv_temp = p.inv_temp;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+            int m, n;
+            tile_coords(p, tile, m, n);
+            const int64_t row = int64_t(m) * kBM + row_in_tile;
+            const int32_t tgt = row < p.T ? __ldg(p.targets + row) : -1;
+            int ok = 1;
+            if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after_sync();
+
+            const int col0 = n * kBN;
+            const int ncols = min(kBN, p.V - col0);
+            const int nchunks = (ncols + 31) >> 5;
+            float run_m = -INFINITY, run_s = 0.0f, zt = 0.0f;
+            int32_t run_a = INT_MAX;
+            const uint32_t t_addr = lane_base + acc * uint32_t(kBN);
+            for (int c = 0; c < nchunks; ++c) {
+                uint32_t r[32];
+                tmem_ld32(t_addr + uint32_t(c * 32), r);
+                tmem_ld_wait();
+                float z[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r[j]) * inv_temp;
+                const int nvalid = ncols - c * 32;
+                if (nvalid < 32) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j >= nvalid) z[j] = -INFINITY;  // columns past V
+                }
+                float cm = z[0];
+                int ca = 0;
+#pragma unroll
+                for (int j = 1; j < 32; ++j)
+                    if (z[j] > cm) {
+                        cm = z[j];
+                        ca = j;
+                    }
+                const float cml = cm * kLog2e;
+                float cs = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) cs += exp2f(fmaf(z[j], kLog2e, -cml));
+                const int cbase = col0 + c * 32;
+                const int rel = tgt - cbase;
+                if (unsigned(rel) < 32u) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j == rel) zt = z[j];
+                }
+                lse_combine(run_m, run_s, run_a, cm, cs, cbase + ca);
+            }
+            // Accumulator buffer fully read: hand it back to the MMA warp.
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (row < p.T)
+                p.partials[row * p.num_n + n] =
+                    make_float4(run_m, run_s, __int_as_float(run_a), zt);
+            if (++acc == kAccBufs) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+int g_configured[64];  // per device: dynamic shared memory attribute set
+
+}  // namespace
+
+cudaError_t launch_lmhead_partials(const CUtensorMap* th, const CUtensorMap* tw,
+                                   const int32_t* targets, void* partials, int64_t T, int64_t V,
+                                   int64_t H, float inv_temp, int num_sms, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && !g_configured[dev]) {
+        e = cudaFuncSetAttribute(lmhead_partials_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        g_configured[dev] = 1;
+    }
+    Args a;
+    a.targets = targets;
+    a.partials = static_cast<float4*>(partials);
+    a.T = T;
+    a.V = int(V);
+    a.num_m = int((T + kBM - 1) / kBM);
+    a.num_n = int((V + kBN - 1) / kBN);
+    a.num_kb = int((H + kBK - 1) / kBK);
+    a.band = a.num_m < 32 ? a.num_m : 32;
+    a.num_tiles = a.num_m * a.num_n;
+    a.inv_temp = inv_temp;
+    const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
+    lmhead_partials_kernel<<<grid, kThreads, kSmemBytes, stream>>>(*th, *tw, a);
+    return cudaGetLastError();
+}
+
+cudaError_t lmhead_take_error(unsigned int* out) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_lmhead_error, sizeof v);
+    if (e != cudaSuccess) return e;
+    if (v) e = cudaMemcpyToSymbol(g_lmhead_error, &zero, sizeof zero);
+    *out = v;
+    return e;
+}
+
+}  // namespace rlk

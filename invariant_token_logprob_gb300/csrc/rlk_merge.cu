@@ -1,0 +1,70 @@
+// rlk_merge.cu -- fixed-tree merge of per-(row, vocabulary tile) partials into
+// the row's LSE, argmax and selected-token logprob.
+//
+// The RL-Kernel blog ("大模型强化学习后训练：如何通过 RL-Kernel 彻底消除训推 LogP
+// 偏差", §七 "LogP") merges per-shard local statistics in a fixed
+// vocabulary-tile order; §四 gives the blockwise LSE merge it relies on.  Here
+// one warp owns one row:
+//   lane l folds tiles l, l+32, l+64, ... left to right (lse_combine), then the
+//   32 lane results meet in a 5-step xor butterfly (16, 8, 4, 2, 1).
+// The tree depends only on NVT = ceil(V / 256), never on T, and lse_combine is
+// commutative bit for bit, so all lanes finish with identical bits.
+//   lse = M + log(S),  argmax = A,  logp = zt(tile of target) - lse
+// (logp = 0 for a target outside [0, V)).
+#include <limits.h>
+
+#include "rlk_internal.h"
+#include "rlk_lse.cuh"
+
+namespace rlk {
+namespace {
+
+constexpr int kMergeWarps = 8;
+
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    lse_merge_kernel(const float4* __restrict__ partials, const int32_t* __restrict__ targets,
+                     int64_t T, int V, int nvt, float* __restrict__ out_logp,
+                     float* __restrict__ out_lse, int32_t* __restrict__ out_argmax) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+    if (row >= T) return;  // whole warp leaves together
+    const float4* pr = partials + row * nvt;
+
+    float m = -INFINITY, s = 0.0f;
+    int32_t a = INT_MAX;
+    for (int j = lane; j < nvt; j += 32) {
+        const float4 q = __ldg(pr + j);
+        lse_combine(m, s, a, q.x, q.y, __float_as_int(q.z));
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+        const float so = __shfl_xor_sync(0xffffffffu, s, off);
+        const int32_t ao = __shfl_xor_sync(0xffffffffu, a, off);
+        lse_combine(m, s, a, mo, so, ao);
+    }
+    if (lane == 0) {
+        const float lse = m + logf(s);
+        const int32_t tgt = __ldg(targets + row);
+        float logp = 0.0f;
+        if (tgt >= 0 && tgt < V) logp = __ldg(pr + tgt / kVocabTile).w - lse;
+        out_logp[row] = logp;
+        out_lse[row] = lse;
+        out_argmax[row] = a;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_lse_merge(const void* partials, const int32_t* targets, int64_t T, int64_t V,
+                             float* out_logp, float* out_lse, int32_t* out_argmax,
+                             cudaStream_t stream) {
+    const int nvt = int((V + kVocabTile - 1) / kVocabTile);
+    const int64_t blocks = (T + kMergeWarps - 1) / kMergeWarps;
+    lse_merge_kernel<<<unsigned(blocks), kMergeWarps * 32, 0, stream>>>(
+        static_cast<const float4*>(partials), targets, T, int(V), nvt, out_logp, out_lse,
+        out_argmax);
+    return cudaGetLastError();
+}
+
+}  // namespace rlk

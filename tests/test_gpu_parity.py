@@ -1,0 +1,206 @@
+"""GPU parity at small sizes: every output of the CUDA path against the fp64
+oracle, element by element, on seeded inputs spanning several tiles and ragged
+tails in T, H and V; plus the degenerate cases (V = 1, W = 0, exact integer
+logits with ties, ignored targets) and the two phases on their own (partials
+vs the oracle's per-block statistics; merge vs the oracle's fp64 merge)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_bitwise, assert_parity, gpu_logprob, to_dev
+from invariant_token_logprob_gb300.inputs import lm_head_inputs, tiny_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import invariant_token_logprob_gb300 as rlk
+    rlk.lib()
+
+
+def test_tiny_full_parity_and_forced_ties(olib):
+    d = tiny_inputs(seed=0, device="cuda")
+    gpu = gpu_logprob(d["h"], d["W"], d["targets"], 1.0)
+    ref = oracle.logprob(d["h"], d["W"], d["targets"], 1.0, lib=olib)
+    assert_parity(gpu, ref, what="tiny")
+    # forced exact ties: the lower vocabulary index wins, on both copies of each row
+    exp = d["expected_tie_argmax"].numpy()
+    src, dst = d["dup_src"].cpu().numpy(), d["dup_dst"].cpu().numpy()
+    assert np.array_equal(gpu[2][src], exp)
+    assert np.array_equal(gpu[2][dst], exp)
+    # the same hidden row at two batch positions: identical lse / argmax bits
+    assert np.array_equal(gpu[1][src].view(np.uint32), gpu[1][dst].view(np.uint32))
+
+
+@pytest.mark.parametrize("T,H,V,seed", [
+    (1, 64, 1, 1), (3, 8, 257, 2), (130, 72, 1000, 3), (257, 136, 2049, 4),
+    (5, 4096, 3000, 5), (129, 512, 512, 6), (300, 64, 33, 7), (2, 1024, 151936, 8),
+])
+def test_ragged_shapes(T, H, V, seed, olib):
+    d = to_dev(lm_head_inputs(T, H, V, seed=seed))
+    it = 1.0 / 0.7 if seed % 2 else 1.0
+    gpu = gpu_logprob(d["h"], d["W"], d["targets"], it)
+    ref = oracle.logprob(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu(), it, lib=olib)
+    assert_parity(gpu, ref, what=f"T={T} H={H} V={V}")
+
+
+def test_zero_weights_closed_form():
+    for V in (1, 1024, 151936):
+        T, H = 7, 64
+        h = torch.randn(T, H, device="cuda").to(torch.bfloat16)
+        W = torch.zeros(V, H, device="cuda", dtype=torch.bfloat16)
+        tg = torch.arange(T, device="cuda", dtype=torch.int32) % V
+        lp, lse, am = gpu_logprob(h, W, tg)
+        lnV = math.log(V)
+        assert np.all(np.abs(lse - lnV) <= 1e-5 * max(1.0, lnV)), lse
+        assert np.all(np.abs(lp + lnV) <= 5e-4)
+        assert np.all(am == 0)
+
+
+def test_exact_integer_logits_and_ties(olib):
+    """Small-integer bf16 inputs make every fp32 logit an exact integer, so the
+    GPU argmax must equal the oracle's lowest-index argmax exactly, ties included."""
+    g = torch.Generator().manual_seed(17)
+    T, H, V = 200, 32, 700
+    h = torch.randint(-3, 4, (T, H), generator=g).to(torch.bfloat16)
+    W = torch.randint(-2, 3, (V, H), generator=g).to(torch.bfloat16)
+    W[650] = W[3]      # duplicated rows: exact ties across vocabulary tiles
+    W[300] = W[299]
+    tg = torch.randint(-1, V, (T,), generator=g, dtype=torch.int32)
+    gpu = gpu_logprob(h.cuda(), W.cuda(), tg.cuda(), 0.5)
+    ref = oracle.logprob(h, W, tg, 0.5, lib=olib)
+    assert np.array_equal(gpu[2], ref["argmax"])
+    assert_parity(gpu, ref, what="integer logits")
+    assert np.all(gpu[0][tg.numpy() < 0] == 0.0)
+
+
+def test_ignored_targets_write_zero(olib):
+    d = lm_head_inputs(16, 64, 600, seed=9)
+    d["targets"][:4] = torch.tensor([-1, 600, -100, 2**31 - 1], dtype=torch.int32)
+    dd = to_dev(d)
+    gpu = gpu_logprob(dd["h"], dd["W"], dd["targets"])
+    assert np.all(gpu[0][:4] == 0.0)
+    ref = oracle.logprob(d["h"], d["W"], d["targets"], lib=olib)
+    assert_parity(gpu, ref, what="ignored targets")
+
+
+def test_temperature_is_one_exact_multiply():
+    """inv_temp = 2 equals doubling W bit for bit (both exact in fp32/bf16)."""
+    d = to_dev(lm_head_inputs(40, 256, 1500, seed=12))
+    a = gpu_logprob(d["h"], d["W"], d["targets"], 2.0)
+    b = gpu_logprob(d["h"], (d["W"].float() * 2).to(torch.bfloat16), d["targets"], 1.0)
+    assert_bitwise(a, b, "inv_temp=2 vs 2W")
+
+
+def test_partials_match_oracle_block_stats(olib):
+    """Phase 1 alone: each (row, 256-column tile) record {m, s, a, zt} against the
+    oracle's per-block statistics."""
+    import invariant_token_logprob_gb300 as rlk
+    T, H, V = 150, 192, 1300
+    d = lm_head_inputs(T, H, V, seed=21)
+    dd = to_dev(d)
+    P = rlk.logprob_partials(dd["h"], dd["W"], dd["targets"], 1.0)
+    rlk.check_device_error()
+    P = P.cpu().numpy()
+    bs = oracle.block_stats(d["h"], d["W"], d["targets"], rlk.vocab_tile(), 1.0, lib=olib)
+    m, s = P[..., 0].astype(np.float64), P[..., 1].astype(np.float64)
+    a, zt = P[..., 2].view(np.int32), P[..., 3].astype(np.float64)
+    assert m.shape == bs["m"].shape
+    assert np.all(np.abs(m - bs["m"]) <= 1e-5 * np.maximum(1, np.abs(bs["m"])))
+    assert np.all(np.abs(s - bs["s"]) <= 1e-5 * bs["s"])
+    assert np.all(np.abs(zt - bs["zt"]) <= 1e-5 * np.maximum(1, np.abs(bs["zt"])))
+    # argmax exact wherever the block's max is clear of the runner-up in the oracle
+    z = (d["h"].double() @ d["W"].double().T).numpy()
+    nb = m.shape[1]
+    for j in range(nb):
+        zz = np.sort(z[:, j * 256:min(V, (j + 1) * 256)], axis=1)
+        clear = (zz[:, -1] - zz[:, -2] > 1e-3) if zz.shape[1] > 1 else np.ones(T, bool)
+        assert np.array_equal(a[clear, j], bs["a"][clear, j])
+
+
+def test_merge_alone_matches_oracle_fp64_merge(olib):
+    """Phase 2 alone on synthetic partials (including -inf blocks and equal maxima)."""
+    import invariant_token_logprob_gb300 as rlk
+    g = np.random.default_rng(4)
+    V = 151936
+    nvt = (V + 255) // 256
+    T = 333
+    m = g.normal(0, 3, (T, nvt)).astype(np.float32)
+    m[:, 5] = m[:, 100]                       # equal maxima in different tiles
+    m[7, :] = 0.0                             # a row where every tile ties
+    m[8, 1:] = -np.inf                        # a row with only one populated tile
+    s = g.uniform(1.0, 256.0, (T, nvt)).astype(np.float32)
+    s[8, 1:] = 0.0
+    a = (np.arange(nvt, dtype=np.int32)[None, :] * 256 + g.integers(0, 128, (T, nvt))).astype(np.int32)
+    zt = g.normal(0, 3, (T, nvt)).astype(np.float32)
+    tg = g.integers(0, V, T).astype(np.int32)
+    tg[:3] = -1
+    P = np.stack([m, s, a.view(np.float32), zt], axis=-1)
+    Pd = torch.from_numpy(P).cuda()
+    lp, lse, am = rlk.lse_merge(Pd, torch.from_numpy(tg).cuda(), V)
+    lp, lse, am = lp.cpu().numpy(), lse.cpu().numpy(), am.cpu().numpy()
+    ref = oracle.merge_blocks(m, s, a, zt, tg, V, 256, lib=olib)
+    assert np.all(np.abs(lse - ref["lse"]) <= 2e-6 * np.maximum(1, np.abs(ref["lse"])))
+    assert np.all(np.abs(lp - ref["logp"]) <= 2e-5)
+    assert np.array_equal(am, ref["argmax"])
+    assert np.all(lp[:3] == 0.0)
+
+
+def test_consistency_stats_match_oracle(olib):
+    import invariant_token_logprob_gb300 as rlk
+    g = np.random.default_rng(8)
+    for n in (1, 1000, 16384, 16385, 100003):
+        b = g.normal(-3, 1, n).astype(np.float32)
+        a = b + (g.normal(0, 1e-3, n) * (g.uniform(size=n) < 0.3)).astype(np.float32)
+        mask = (g.uniform(size=n) > 0.1).astype(np.int8)
+        for mk in (None, mask):
+            st = rlk.consistency_stats(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(),
+                                       None if mk is None else torch.from_numpy(mk).cuda())
+            ref = oracle.consistency_stats(a, b, mk, lib=olib)
+            got = np.array([st[k] for k in rlk.STAT_NAMES])
+            assert got[0] == ref[0]
+            assert np.allclose(got[1:5], ref[1:5], rtol=1e-9, atol=1e-15)
+            assert np.array_equal(got[5:], ref[5:])
+    # diff = 0: identical inputs give all-zero statistics
+    x = torch.randn(5000, device="cuda")
+    st = rlk.consistency_stats(x, x.clone())
+    assert all(st[k] == 0.0 for k in ("max_abs", "mean_abs", "std_abs", "k3_mean", "sum_delta",
+                                      "n_bit_mismatch"))
+    assert st["first_mismatch"] == -1.0 and st["n_valid"] == 5000
+
+
+def test_chunking_permutation_and_repeat_invariance_small():
+    """Bitwise: the tiny workload as one call, in every chunk size 1..64, in a
+    permuted order, and repeated, gives identical bits for every row."""
+    d = tiny_inputs(seed=0, device="cuda")
+    h, W, tg = d["h"], d["W"], d["targets"]
+    T = h.shape[0]
+    full = gpu_logprob(h, W, tg)
+    for c in range(1, T + 1):
+        parts = [gpu_logprob(h[i:i + c].contiguous(), W, tg[i:i + c].contiguous())
+                 for i in range(0, T, c)]
+        got = tuple(np.concatenate([p[k] for p in parts]) for k in range(3))
+        assert_bitwise(full, got, f"chunk={c}")
+    perm = torch.randperm(T, generator=torch.Generator().manual_seed(5)).cuda()
+    pg = gpu_logprob(h[perm].contiguous(), W, tg[perm].contiguous())
+    inv = torch.argsort(perm).cpu().numpy()
+    assert_bitwise(full, tuple(x[inv] for x in pg), "permuted rows")
+    for _ in range(3):
+        assert_bitwise(full, gpu_logprob(h, W, tg), "repeat")
+
+
+def test_padding_rows_do_not_leak():
+    """A row's bits do not depend on what else shares its 128-row tile."""
+    d = lm_head_inputs(128, 256, 3000, seed=31)
+    dd = to_dev(d)
+    base = gpu_logprob(dd["h"], dd["W"], dd["targets"])
+    h2 = dd["h"].clone()
+    h2[1:] = (h2[1:].float() * -7.0).to(torch.bfloat16)  # change every other row
+    other = gpu_logprob(h2, dd["W"], dd["targets"])
+    assert_bitwise(tuple(x[:1] for x in base), tuple(x[:1] for x in other), "row 0 neighbours")
