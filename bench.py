@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of the batch-invariant selected-token logprob on GB300.
+
+Workload (one "step" = one pass of the whole path over one batch):
+  Qwen3-8B-shaped LM head, training recompute: T = 4096 rows (8 packed
+  sequences of 512), H = 4096, V = 151936, RMS-normalised bf16 hidden states,
+  W ~ N(0, 0.02) bf16, uniform int32 targets, inv_temp = 1.0, 10% of the
+  tokens masked out of the acceptance statistics.  Synthetic and seeded: no
+  model weights or datasets exist here.
+  Step = rlk_logprob_partials (fused tcgen05 GEMM + vocabulary-tile epilogue)
+       -> rlk_lse_merge (fixed-tree merge)
+       -> rlk_consistency_stats against a stored "rollout" logprob vector
+          (synchronous: the acceptance check of every step).
+  W alone is 1.245 GB, ten times L2 (129 MB), so inputs are larger than L2 and
+  no flush is needed between steps.
+
+Printed (rank 0, one JSON line): device-timed tokens/s over the whole job,
+e2e tokens/s through rlk_logprob with pinned host buffers (H2D of h and
+targets, D2H of logp/lse/argmax inside the timed region; W stays resident as
+model weights do), the dominant kernel's roofline from live CUDA events, SM
+clocks sampled during the timed region, the CPU oracle's throughput on a
+bounded sample, and decode-regime points (T = 1, 16: HBM-bound).
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on the host cores, each step a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+T_CFG, H_CFG, V_CFG = 4096, 4096, 151936
+METRIC = "tokens/s of batch-invariant logprob (H=4096,V=151936); % of TC/HBM roofline"
+WORKLOAD = "Qwen3-8B LM head, training recompute: T=4096 (8 packed x 512), H=4096, V=151936"
+KERNEL_SOURCES = ["invariant_token_logprob_gb300/csrc/rlk_lmhead.cu",
+                  "invariant_token_logprob_gb300/csrc/rlk_sm103.cuh",
+                  "invariant_token_logprob_gb300/csrc/rlk_lse.cuh",
+                  "invariant_token_logprob_gb300/csrc/rlk_internal.h"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lmhead_partials_T4096_H4096_V151936.md")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-decode", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the LM-head kernel from the committed ncu summary,
+    if that capture was taken of the kernel sources as they are now."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    import re
+    text = open(TRAFFIC_FILE).read()
+    mh = re.search(r"^kernel_hash:\s*([0-9a-f]+)\s*$", text, re.M)
+    mt = re.search(r"^traffic_bytes_per_launch:\s*([0-9]+)\s*$", text, re.M)
+    if not mh or not mt or mh.group(1) != kernel_hash():
+        return None
+    return dict(bytes_per_launch=int(mt.group(1)), source=os.path.relpath(TRAFFIC_FILE, ROOT))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, "t_" + which, time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for t, line in self.samples:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(t=t, sm=float(f[1]), smax=float(f[2]), active=f[4],
+                                 hw=f[5], hwt=f[6], swt=f[7], pcap=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        inwin = [r for r in rows if self.t_start and self.t_stop and self.t_start <= r["t"] <= self.t_stop]
+        window = "timed"
+        if len(inwin) < 3:  # very short timed region: fall back to all samples under load
+            inwin = [r for r in rows if r["sm"] > 0.5 * r["smax"]] or rows
+            window = "warmup+timed"
+        reasons = set()
+        for r in inwin:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return dict(sm_mhz=statistics.median(r["sm"] for r in inwin),
+                    sm_max_mhz=max(r["smax"] for r in inwin), reasons=sorted(reasons),
+                    samples=len(inwin), window=window)
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(d, rows_per_thread=8):
+    """Time the oracle as it stands on a bounded sample of rows of the workload."""
+    import numpy as np
+    import oracle
+    lib = oracle.load()
+    threads = oracle.num_threads(lib)
+    n = max(1, rows_per_thread * threads)
+    g = np.random.default_rng(1234)
+    rows = np.sort(g.choice(d["h"].shape[0], size=min(n, d["h"].shape[0]), replace=False))
+    h = d["h"].cpu()
+    W = d["W"].cpu()
+    tg = d["targets"].cpu()
+    t0 = time.perf_counter()
+    oracle.logprob(h, W, tg, 1.0, rows=rows, lib=lib)
+    dt = time.perf_counter() - t0
+    return dict(value=len(rows) / dt, unit="tokens/s", cores=threads, kind="oracle",
+                sample=f"{len(rows)} seeded rows of the T=4096 batch (full V=151936, H=4096), "
+                       f"fp64 oracle, OpenMP over rows, {dt:.1f} s")
+
+
+def run_reference(args):
+    world, rank, local = dist_init()
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    from invariant_token_logprob_gb300.inputs import lm_head_inputs
+    lib = oracle.load()
+    threads = oracle.num_threads(lib)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    d = lm_head_inputs(T_CFG, H_CFG, V_CFG, seed=1000, device=dev, hidden="rms", mask_zero_frac=0.1)
+    h, W, tg = d["h"].cpu(), d["W"].cpu(), d["targets"].cpu()
+    rows_per_step = threads  # one row per core per step: about a second a step
+    import numpy as np
+    g = np.random.default_rng(7)
+    times = []
+    for i in range(args.warmup + args.steps):
+        rows = np.sort(g.choice(T_CFG, size=rows_per_step, replace=False))
+        t0 = time.perf_counter()
+        oracle.logprob(h, W, tg, 1.0, rows=rows, lib=lib)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = rows_per_step * len(times) / total
+    line = dict(impl="reference", metric=METRIC, value=value, unit="tokens/s", n_gpus=args.gpus,
+                steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * total / len(times),
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic",
+                config=dict(workload=WORKLOAD, T=T_CFG, H=H_CFG, V=V_CFG, inv_temp=1.0,
+                            step=f"oracle over {rows_per_step} seeded rows of the batch"),
+                cpu_baseline=dict(value=value, unit="tokens/s", cores=threads, kind="oracle",
+                                  sample=f"{rows_per_step} rows per step, full V and H"),
+                e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_decode(rlk, torch, W, T, reps, stream):
+    """Device time per call of the whole path at a small T (weight streaming)."""
+    h = torch.randn(T, H_CFG, device=W.device).to(torch.bfloat16)
+    tg = torch.randint(0, V_CFG, (T,), device=W.device, dtype=torch.int32)
+    out = [torch.empty(T, device=W.device, dtype=dt) for dt in (torch.float32, torch.float32, torch.int32)]
+    for _ in range(5):
+        rlk.logprob(h, W, tg, 1.0, out=out)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        rlk.logprob(h, W, tg, 1.0, out=out)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps * 1e-3
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    world, rank, local = dist_init()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py (ours) needs a CUDA device: the library has no CPU path")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import invariant_token_logprob_gb300 as rlk
+    from invariant_token_logprob_gb300.inputs import lm_head_inputs
+    rlk.lib()
+    pk = peaks()
+
+    # ---------------------------------------------------------------- inputs
+    d = lm_head_inputs(T_CFG, H_CFG, V_CFG, seed=1000 + rank, device=dev, hidden="rms",
+                       mask_zero_frac=0.1)
+    h, W, tg, mask = d["h"], d["W"], d["targets"], d["mask"]
+    T, H, V = T_CFG, H_CFG, V_CFG
+    nvt = (V + rlk.vocab_tile() - 1) // rlk.vocab_tile()
+    partials = torch.empty((T, nvt, 4), dtype=torch.float32, device=dev)
+    out = [torch.empty(T, device=dev, dtype=dt) for dt in (torch.float32, torch.float32, torch.int32)]
+    stream = torch.cuda.current_stream(dev)
+    # the "rollout" logprobs the acceptance statistics compare against
+    rollout = rlk.logprob(h, W, tg, 1.0)[0].clone()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        rlk.logprob_partials(h, W, tg, 1.0, out=partials)
+        if ev is not None:
+            ev[1].record(stream)
+        rlk.lse_merge(partials, tg, V, out=out)
+        st = rlk.consistency_stats(out[0], rollout, mask)  # synchronous
+        return st
+
+    for _ in range(max(3, args.warmup)):
+        st = step()
+    assert st["n_bit_mismatch"] == 0, "step outputs drifted from the first call"
+    rlk.check_device_error()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark("start")
+    t_start.record(stream)
+    mism = 0
+    for i in range(args.steps):
+        st = step(evs[i])
+        mism += int(st["n_bit_mismatch"])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("stop")
+    barrier(world)
+    clocks.stop()
+    rlk.check_device_error()
+    elapsed = t_start.elapsed_time(t_end) * 1e-3
+    elapsed = max_over_ranks(elapsed, world, dev)
+    gemm_s = [a.elapsed_time(b) * 1e-3 for a, b in evs]
+    gemm_avg = sum(gemm_s) / len(gemm_s)
+    tokens = T * args.steps * world
+    value = tokens / elapsed
+
+    # ---------------------------------------------------------------- e2e
+    h_host = h.cpu().pin_memory()
+    tg_host = tg.cpu().pin_memory()
+    outs_host = [torch.empty(T, dtype=dt).pin_memory() for dt in (torch.float32, torch.float32, torch.int32)]
+    h_dev = torch.empty_like(h)
+    tg_dev = torch.empty_like(tg)
+    e2e_steps = max(3, min(args.steps, 100))
+
+    def e2e_step():
+        h_dev.copy_(h_host, non_blocking=True)
+        tg_dev.copy_(tg_host, non_blocking=True)
+        lp, lse, am = rlk.logprob(h_dev, W, tg_dev, 1.0, out=out)
+        for o, oh in zip((lp, lse, am), outs_host):
+            oh.copy_(o, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_el = max_over_ranks(time.perf_counter() - t0, world, dev)
+    assert np.array_equal(outs_host[0].numpy().view(np.uint32), out[0].cpu().numpy().view(np.uint32))
+    e2e = dict(value=T * e2e_steps * world / e2e_el, unit="tokens/s",
+               h2d_bytes_per_step=int(h.numel() * 2 + tg.numel() * 4),
+               d2h_bytes_per_step=int(T * 12))
+
+    # ---------------------------------------------------------------- regimes
+    decode = None
+    if not args.no_decode:
+        decode = {}
+        wbytes = V * H * 2
+        for Td in (1, 16):
+            s = time_decode(rlk, torch, W, Td, 50, stream)
+            decode[f"T{Td}"] = dict(tokens_per_s=Td / s, us_per_call=s * 1e6,
+                                    hbm_gbs=wbytes / s / 1e9,
+                                    hbm_frac=wbytes / s / 1e9 / pk["hbm_gbs"])
+
+    if rank != 0:
+        return 0
+
+    flops = 2.0 * T * H * V
+    achieved = flops / gemm_avg / 1e12
+    tr = recorded_traffic()
+    roofline = dict(bound="tensor", achieved=achieved, peak=pk["bf16_tflops"], unit="TFLOP/s",
+                    frac=achieved / pk["bf16_tflops"],
+                    peak_source=f"bf16_tflops burst, {pk['source']} (MEASURED_PEAKS.json)"
+                    if pk["source"] == "measured" else "fallback 1.9 PFLOP/s",
+                    traffic=(tr["bytes_per_launch"] if tr else None),
+                    algorithmic_flops_per_launch=flops,
+                    kernel="lmhead_partials_kernel", launch_avg_us=gemm_avg * 1e6,
+                    step_share=gemm_avg * args.steps / (elapsed if world == 1 else elapsed))
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_oracle_sample(d)
+    clk = clocks.summary()
+    line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
+                warmup=args.warmup, ms_per_step=1e3 * elapsed / args.steps,
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+                data="synthetic",
+                config=dict(workload=WORKLOAD, T=T, H=H, V=V, inv_temp=1.0, masked_frac=0.1,
+                            l2="inputs larger than L2 (W 1.245 GB vs 129 MB L2): no flush",
+                            step="partials (fused GEMM+epilogue) -> merge -> consistency stats",
+                            parallelism=f"dp{world} (rows; no collective)"),
+                roofline=roofline, cpu_baseline=cpu, e2e=e2e,
+                gpu_launches=4 * args.steps,
+                clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"],
+                            reasons=clk["reasons"], samples=clk["samples"],
+                            window=clk.get("window")),
+                decode=decode, bitwise_mismatch_vs_first_call=mism)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
