@@ -177,6 +177,37 @@ rlk_status rlk_consistency_stats(const float *logp_a, const float *logp_b,
                                  rlk_stream_t stream);
 
 /*
+ * rlk_logprob for callers that cannot allocate device memory.  The pages
+ * describe no counterpart of this entry point; it exists for this library's
+ * users.  Callers that cannot allocate include code running under CUDA-graph
+ * capture, engines whose device memory is pre-reserved by their own allocator,
+ * and decode loops that must never block on an allocation; they may also have
+ * no spare buffer to pass to rlk_logprob_ws.
+ *
+ * Same arguments, results and bits as rlk_logprob (inputs and outputs are still
+ * the caller's).  Instead of a workspace, the partials live in one fixed device
+ * array of RLK_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library keeps for the life of the process.
+ *   Limit: T * ceil(V / rlk_vocab_tile()) * 16 <= RLK_NOALLOC_SCRATCH_BYTES, i.e.
+ *   up to 1765 rows per call at V = 151936; larger problems return
+ *   RLK_ERR_WORKSPACE before anything is launched (split the rows into calls).
+ *   Allocates nothing: no cudaMalloc / cudaFree or allocating library routine.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Sharing: every call on a device uses the same array and leaves its
+ *   contents behind (nothing in it needs to start at zero).  Calls whose
+ *   execution overlaps on the GPU -- on different streams, or from different
+ *   host threads -- race on the array and give undefined results; serialise
+ *   them (e.g. one stream).
+ */
+#define RLK_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+rlk_status rlk_logprob_noalloc(const void *hidden_bf16, const void *weight_bf16,
+                               const int32_t *targets_i32, int64_t T, int64_t H, int64_t V,
+                               float inv_temp, float *out_logp_f32, float *out_lse_f32,
+                               int32_t *out_argmax_i32, rlk_stream_t stream);
+
+/*
  * Every device-side wait in the library's kernels is bounded in time.  If one
  * runs out, the kernel records it in a per-device error word, drains its own
  * in-flight copies, releases its tensor memory and returns (its outputs are
