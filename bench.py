@@ -55,6 +55,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--decode-only", action="store_true",
+                   help="time only the decode regime at T = --decode-T (for profiling)")
+    p.add_argument("--decode-T", type=int, default=1)
     return p.parse_args()
 
 
@@ -247,21 +250,58 @@ def run_reference(args):
     return 0
 
 
-def time_decode(rlk, torch, W, T, reps, stream):
-    """Device time per call of the whole path at a small T (weight streaming)."""
-    h = torch.randn(T, H_CFG, device=W.device).to(torch.bfloat16)
-    tg = torch.randint(0, V_CFG, (T,), device=W.device, dtype=torch.int32)
-    out = [torch.empty(T, device=W.device, dtype=dt) for dt in (torch.float32, torch.float32, torch.int32)]
-    for _ in range(5):
-        rlk.logprob(h, W, tg, 1.0, out=out)
+def time_decode(rlk, torch, W, Ts, reps, rounds, stream):
+    """Device time per call of the whole path at small T (weight streaming).
+    The T values are interleaved over `rounds` rounds and the median per-call
+    time of each T is kept, so no T is measured only in one clock state."""
+    cases = {}
+    for T in Ts:
+        h = torch.randn(T, H_CFG, device=W.device).to(torch.bfloat16)
+        tg = torch.randint(0, V_CFG, (T,), device=W.device, dtype=torch.int32)
+        out = [torch.empty(T, device=W.device, dtype=dt)
+               for dt in (torch.float32, torch.float32, torch.int32)]
+        cases[T] = (h, tg, out)
+        for _ in range(3):
+            rlk.logprob(h, W, tg, 1.0, out=out)
+    times = {T: [] for T in Ts}
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(reps):
-        rlk.logprob(h, W, tg, 1.0, out=out)
-    e1.record(stream)
-    e1.synchronize()
-    return e0.elapsed_time(e1) / reps * 1e-3
+    for _ in range(rounds):
+        for T in Ts:
+            h, tg, out = cases[T]
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                rlk.logprob(h, W, tg, 1.0, out=out)
+            e1.record(stream)
+            e1.synchronize()
+            times[T].append(e0.elapsed_time(e1) / reps * 1e-3)
+    return {T: statistics.median(v) for T, v in times.items()}
+
+
+def decode_points(rlk, torch, W, stream, pk, Ts=(1, 2, 4, 8, 16), reps=50, rounds=3):
+    wbytes = V_CFG * H_CFG * 2
+    res = {}
+    for T, s in time_decode(rlk, torch, W, Ts, reps, rounds, stream).items():
+        res[f"T{T}"] = dict(tokens_per_s=T / s, us_per_call=s * 1e6, hbm_gbs=wbytes / s / 1e9,
+                            hbm_frac=wbytes / s / 1e9 / pk["hbm_gbs"])
+    return res
+
+
+def run_decode_only(args):
+    """Decode regime alone (T = --decode-T rows per call, H=4096, V=151936): used
+    for profiling the weight-streaming regime; prints one JSON line."""
+    import torch
+    import invariant_token_logprob_gb300 as rlk
+    torch.cuda.set_device(0)
+    pk = peaks()
+    g = torch.Generator(device="cuda").manual_seed(1000)
+    W = (torch.randn(V_CFG, H_CFG, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    res = decode_points(rlk, torch, W, stream, pk, Ts=(args.decode_T,), reps=args.steps,
+                        rounds=1)
+    rlk.check_device_error()
+    print(json.dumps(dict(mode="decode-only", H=H_CFG, V=V_CFG, **res)), flush=True)
+    return 0
 
 
 def run_ours(args):
@@ -363,13 +403,7 @@ def run_ours(args):
     # ---------------------------------------------------------------- regimes
     decode = None
     if not args.no_decode:
-        decode = {}
-        wbytes = V * H * 2
-        for Td in (1, 16):
-            s = time_decode(rlk, torch, W, Td, 50, stream)
-            decode[f"T{Td}"] = dict(tokens_per_s=Td / s, us_per_call=s * 1e6,
-                                    hbm_gbs=wbytes / s / 1e9,
-                                    hbm_frac=wbytes / s / 1e9 / pk["hbm_gbs"])
+        decode = decode_points(rlk, torch, W, stream, pk)
 
     if rank != 0:
         return 0
@@ -411,6 +445,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.decode_only:
+        return run_decode_only(args)
     return run_ours(args)
 
 

@@ -92,8 +92,11 @@ int rlk_row_tile(void);
 int rlk_vocab_tile(void);
 
 /* Bytes of workspace rlk_logprob_ws needs: T * ceil(V / rlk_vocab_tile()) *
- * sizeof(rlk_partial).  Returns 0 for T <= 0 or V <= 0. */
-size_t rlk_logprob_workspace_size(int64_t T, int64_t V);
+ * sizeof(rlk_partial) for the partials, plus 16 * H * 2 when T < 16 (calls with
+ * fewer than 16 rows stage their hidden rows in a zero-padded 16-row copy, which
+ * streams W faster; the results are bit-identical either way).  Returns 0 for
+ * T <= 0, H <= 0 or V <= 0. */
+size_t rlk_logprob_workspace_size(int64_t T, int64_t H, int64_t V);
 
 /*
  * Selected-token logprob, LSE and argmax for T rows.
@@ -117,7 +120,7 @@ rlk_status rlk_logprob(const void *hidden_bf16, const void *weight_bf16,
                        int32_t *out_argmax_i32, rlk_stream_t stream);
 
 /* Same as rlk_logprob with a caller-owned device workspace of at least
- * rlk_logprob_workspace_size(T, V) bytes, 16-byte aligned (else
+ * rlk_logprob_workspace_size(T, H, V) bytes, 16-byte aligned (else
  * RLK_ERR_WORKSPACE / RLK_ERR_ALIGNMENT).  Allocates nothing. */
 rlk_status rlk_logprob_ws(const void *hidden_bf16, const void *weight_bf16,
                           const int32_t *targets_i32, int64_t T, int64_t H, int64_t V,
@@ -130,8 +133,9 @@ rlk_status rlk_logprob_ws(const void *hidden_bf16, const void *weight_bf16,
  * (per-block max / exp-sum of the RL-Kernel blog §四, taken per fixed tile).
  * Writes partials[t * NVT + j] for every row t < T and tile j < NVT =
  * ceil(V / rlk_vocab_tile()); logits are never written to memory.
- *   partials  device, 16-byte aligned, partials_bytes >= rlk_logprob_workspace_size(T, V)
- * Other arguments as rlk_logprob.
+ *   partials  device, 16-byte aligned, partials_bytes >= T * NVT * sizeof(rlk_partial)
+ * Other arguments as rlk_logprob.  (No small-T staging copy here: the partials
+ * are bit-identical to those rlk_logprob computes, only possibly slower for T < 16.)
  */
 rlk_status rlk_logprob_partials(const void *hidden_bf16, const void *weight_bf16,
                                 const int32_t *targets_i32, int64_t T, int64_t H, int64_t V,
@@ -188,7 +192,7 @@ rlk_status rlk_consistency_stats(const float *logp_a, const float *logp_b,
  * the caller's).  Instead of a workspace, the partials live in one fixed device
  * array of RLK_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
  * loads the library keeps for the life of the process.
- *   Limit: T * ceil(V / rlk_vocab_tile()) * 16 <= RLK_NOALLOC_SCRATCH_BYTES, i.e.
+ *   Limit: rlk_logprob_workspace_size(T, H, V) <= RLK_NOALLOC_SCRATCH_BYTES, i.e.
  *   up to 1765 rows per call at V = 151936; larger problems return
  *   RLK_ERR_WORKSPACE before anything is launched (split the rows into calls).
  *   Allocates nothing: no cudaMalloc / cudaFree or allocating library routine.

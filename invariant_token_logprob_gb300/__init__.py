@@ -62,7 +62,7 @@ def lib() -> ctypes.CDLL:
         L.rlk_vocab_tile.restype = ctypes.c_int
         L.rlk_vocab_tile.argtypes = []
         L.rlk_logprob_workspace_size.restype = sz
-        L.rlk_logprob_workspace_size.argtypes = [i64, i64]
+        L.rlk_logprob_workspace_size.argtypes = [i64, i64, i64]
         L.rlk_logprob.restype = st
         L.rlk_logprob.argtypes = [P, P, P, i64, i64, i64, f32, P, P, P, P]
         L.rlk_logprob_ws.restype = st
@@ -126,8 +126,8 @@ def vocab_tile() -> int:
     return lib().rlk_vocab_tile()
 
 
-def workspace_size(T: int, V: int) -> int:
-    return lib().rlk_logprob_workspace_size(int(T), int(V))
+def workspace_size(T: int, H: int, V: int) -> int:
+    return lib().rlk_logprob_workspace_size(int(T), int(H), int(V))
 
 
 def _check_inputs(h, W, targets):

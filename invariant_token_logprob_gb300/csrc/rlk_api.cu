@@ -140,11 +140,24 @@ rlk_status check_outputs(const float* lp, const float* lse, const int32_t* am) {
     return RLK_OK;
 }
 
+size_t partial_bytes(int64_t T, int64_t V) {
+    return size_t(T) * size_t(num_vocab_tiles(V)) * sizeof(rlk_partial);
+}
+
+// pad_buf: NULL, or (T < kMinTmaRows) room for kMinTmaRows zero-padded h rows.
 rlk_status launch_partials(const void* h, const void* W, const int32_t* tg, int64_t T,
                            int64_t H, int64_t V, float inv_temp, void* partials, int num_sms,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, void* pad_buf = nullptr) {
+    int64_t h_rows = T;
+    if (pad_buf) {
+        cudaError_t e = rlk::launch_pad_rows(h, T, H, pad_buf, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        h = pad_buf;
+        h_rows = rlk::kMinTmaRows;
+    }
     CUtensorMap th, tw;
-    if (!encode_bf16_2d(&th, h, T, H, kRowTile) || !encode_bf16_2d(&tw, W, V, H, kVocabTile))
+    if (!encode_bf16_2d(&th, h, h_rows, H, kRowTile) ||
+        !encode_bf16_2d(&tw, W, V, H, kVocabTile))
         return RLK_ERR_CUDA;
     return from_cuda(rlk::launch_lmhead_partials(&th, &tw, tg, partials, T, V, H, inv_temp,
                                                  num_sms, stream));
@@ -173,9 +186,11 @@ const char* rlk_status_string(int status) {
 int rlk_row_tile(void) { return kRowTile; }
 int rlk_vocab_tile(void) { return kVocabTile; }
 
-size_t rlk_logprob_workspace_size(int64_t T, int64_t V) {
-    if (T <= 0 || V <= 0) return 0;
-    return size_t(T) * size_t(num_vocab_tiles(V)) * sizeof(rlk_partial);
+size_t rlk_logprob_workspace_size(int64_t T, int64_t H, int64_t V) {
+    if (T <= 0 || V <= 0 || H <= 0) return 0;
+    size_t bytes = partial_bytes(T, V);
+    if (T < rlk::kMinTmaRows) bytes += size_t(rlk::kMinTmaRows) * size_t(H) * 2;
+    return bytes;
 }
 
 rlk_status rlk_logprob_partials(const void* hidden_bf16, const void* weight_bf16,
@@ -188,7 +203,7 @@ rlk_status rlk_logprob_partials(const void* hidden_bf16, const void* weight_bf16
     if ((st = check_operands(hidden_bf16, weight_bf16, targets_i32, H)) != RLK_OK) return st;
     if (!partials) return RLK_ERR_INVALID_ARG;
     if (!aligned16(partials)) return RLK_ERR_ALIGNMENT;
-    if (partials_bytes < rlk_logprob_workspace_size(T, V)) return RLK_ERR_WORKSPACE;
+    if (partials_bytes < partial_bytes(T, V)) return RLK_ERR_WORKSPACE;
     int dev, sms;
     if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
     return launch_partials(hidden_bf16, weight_bf16, targets_i32, T, H, V, inv_temp, partials,
@@ -222,12 +237,13 @@ rlk_status rlk_logprob_ws(const void* hidden_bf16, const void* weight_bf16,
     if ((st = check_outputs(out_logp_f32, out_lse_f32, out_argmax_i32)) != RLK_OK) return st;
     if (!workspace) return RLK_ERR_WORKSPACE;
     if (!aligned16(workspace)) return RLK_ERR_ALIGNMENT;
-    if (workspace_bytes < rlk_logprob_workspace_size(T, V)) return RLK_ERR_WORKSPACE;
+    if (workspace_bytes < rlk_logprob_workspace_size(T, H, V)) return RLK_ERR_WORKSPACE;
     int dev, sms;
     if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void* pad = T < rlk::kMinTmaRows ? static_cast<char*>(workspace) + partial_bytes(T, V) : nullptr;
     st = launch_partials(hidden_bf16, weight_bf16, targets_i32, T, H, V, inv_temp, workspace, sms,
-                         s);
+                         s, pad);
     if (st != RLK_OK) return st;
     return from_cuda(rlk::launch_lse_merge(workspace, targets_i32, T, V, out_logp_f32,
                                            out_lse_f32, out_argmax_i32, s));
@@ -245,7 +261,7 @@ rlk_status rlk_logprob(const void* hidden_bf16, const void* weight_bf16,
     int dev, sms;
     if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const size_t need = rlk_logprob_workspace_size(T, V);
+    const size_t need = rlk_logprob_workspace_size(T, H, V);
     void* ws = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -270,7 +286,8 @@ rlk_status rlk_logprob(const void* hidden_bf16, const void* weight_bf16,
         }
         ws = w.ptr;
     }
-    st = launch_partials(hidden_bf16, weight_bf16, targets_i32, T, H, V, inv_temp, ws, sms, s);
+    void* pad = T < rlk::kMinTmaRows ? static_cast<char*>(ws) + partial_bytes(T, V) : nullptr;
+    st = launch_partials(hidden_bf16, weight_bf16, targets_i32, T, H, V, inv_temp, ws, sms, s, pad);
     if (st != RLK_OK) return st;
     return from_cuda(rlk::launch_lse_merge(ws, targets_i32, T, V, out_logp_f32, out_lse_f32,
                                            out_argmax_i32, s));

@@ -13,6 +13,13 @@ constexpr int kRowTile = 128;    // rows per tile  = UMMA M
 constexpr int kVocabTile = 256;  // columns per tile = UMMA N
 constexpr int kKBlock = 64;      // K elements per pipeline stage (one 128-B swizzle row)
 
+// Calls with fewer rows than this get their h rows copied into a zero-padded
+// buffer of this many rows before the LM-head kernel runs (see rlk_pad.cu).
+constexpr int kMinTmaRows = 16;
+
+// Copy h [T][H] (T < kMinTmaRows) into dst [kMinTmaRows][H], zeros past row T.
+cudaError_t launch_pad_rows(const void* h, int64_t T, int64_t H, void* dst, cudaStream_t stream);
+
 // Fused LM-head GEMM + vocabulary-tile epilogue.  Writes partials[T][NVT]
 // (16-byte records {m, s, a, zt}).  th / tw are 2-D tensor maps of h [T,H] and
 // W [V,H] with boxes {kKBlock, kRowTile} / {kKBlock, kVocabTile}, 128-B swizzle.

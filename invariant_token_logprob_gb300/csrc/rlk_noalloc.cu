@@ -46,10 +46,10 @@ extern "C" rlk_status rlk_logprob_noalloc(const void* hidden_bf16, const void* w
                                           int64_t V, float inv_temp, float* out_logp_f32,
                                           float* out_lse_f32, int32_t* out_argmax_i32,
                                           rlk_stream_t stream) {
-    if (T < 0 || V < 1 || V > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    if (T < 0 || H < 1 || V < 1 || V > INT32_MAX) return RLK_ERR_INVALID_ARG;
     if (T == 0) return RLK_OK;
     // Refuse, before touching the device, any problem whose partials do not fit.
-    if (rlk_logprob_workspace_size(T, V) > kScratchBytes) return RLK_ERR_WORKSPACE;
+    if (rlk_logprob_workspace_size(T, H, V) > kScratchBytes) return RLK_ERR_WORKSPACE;
 
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {

@@ -204,3 +204,21 @@ def test_padding_rows_do_not_leak():
     h2[1:] = (h2[1:].float() * -7.0).to(torch.bfloat16)  # change every other row
     other = gpu_logprob(h2, dd["W"], dd["targets"])
     assert_bitwise(tuple(x[:1] for x in base), tuple(x[:1] for x in other), "row 0 neighbours")
+
+
+@pytest.mark.parametrize("T", [1, 5, 15, 16, 17, 40])
+def test_caller_workspace_matches_cached_workspace(T):
+    """rlk_logprob_ws with an exactly-sized caller workspace (including the
+    zero-padded 16-row staging copy below 16 rows) gives rlk_logprob's bits; one
+    byte less is refused before anything runs."""
+    import invariant_token_logprob_gb300 as rlk
+    d = to_dev(lm_head_inputs(T, 256, 3000, seed=50 + T))
+    need = rlk.workspace_size(T, 256, 3000)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    a = rlk.logprob_ws(d["h"], d["W"], d["targets"], ws)
+    b = rlk.logprob(d["h"], d["W"], d["targets"])
+    rlk.check_device_error()
+    assert_bitwise(tuple(x.cpu().numpy() for x in a), tuple(x.cpu().numpy() for x in b), f"T={T}")
+    with pytest.raises(rlk.RlkError) as ei:
+        rlk.logprob_ws(d["h"], d["W"], d["targets"], ws[:need - 1])
+    assert ei.value.status == 5
