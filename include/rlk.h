@@ -161,6 +161,37 @@ rlk_status rlk_lse_merge(const rlk_partial *partials, const int32_t *targets_i32
                          int32_t *out_argmax_i32, rlk_stream_t stream);
 
 /*
+ * Backward of the selected-token logprob (the training half of the method:
+ * "Finish RL Training Faster: Bitwise-Consistent, High-Performance,
+ * Agent-Driven", section "核心设计范式：推理算子定义数值基准，训练仅挂接反向求导" --
+ * the forward values come from the inference kernel, the training side adds
+ * the derivative).  With p = softmax(z) and g = grad_logp:
+ *   dz[t][v]  = g[t] * ([v == target[t]] - p[t][v])      (0 for ignored rows)
+ *   grad_h    = inv_temp * dz . W         [T][H] fp32 (overwritten)
+ *   grad_W    = inv_temp * dz^T . h       [V][H] fp32 (overwritten, or added to
+ *                                          when accumulate_grad_weight != 0)
+ * The logits are recomputed on the forward's fixed tiles (same main loop, so
+ * the same fp32 logits), p uses the forward's lse, dz is rounded once to bf16
+ * and the two products run as bf16 x bf16 -> fp32 library GEMMs.
+ *   lse_f32        device [T]: the forward's lse output
+ *   grad_logp_f32  device [T]: upstream gradient of each logp
+ *   grad_hidden_f32, grad_weight_f32: device, may be NULL (that product is skipped)
+ *   workspace      device, 16-byte aligned, >= rlk_logprob_backward_workspace_size
+ *                  bytes; holds dz as bf16 [T][V] row-major at offset 0 on return
+ * Other arguments and conditions as rlk_logprob.  Asynchronous on `stream`.
+ * The first call on a device creates a cuBLAS handle (kept until rlk_shutdown).
+ * Deterministic run to run; unlike the forward, the gradients are not promised
+ * to be independent of T (they are sums over rows and over the vocabulary).
+ */
+size_t rlk_logprob_backward_workspace_size(int64_t T, int64_t H, int64_t V);
+rlk_status rlk_logprob_backward(const void *hidden_bf16, const void *weight_bf16,
+                                const int32_t *targets_i32, const float *lse_f32,
+                                const float *grad_logp_f32, int64_t T, int64_t H, int64_t V,
+                                float inv_temp, float *grad_hidden_f32, float *grad_weight_f32,
+                                int accumulate_grad_weight, void *workspace,
+                                size_t workspace_bytes, rlk_stream_t stream);
+
+/*
  * Acceptance statistics between two logprob vectors ("Finish RL Training
  * Faster ...", paragraph "diff = 0 的数学定义": max, mean and std of
  * |p_rollout - p_train| and the k3 KL r - 1 - log r).  a = train logp,

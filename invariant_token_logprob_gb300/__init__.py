@@ -18,6 +18,7 @@ from typing import Optional
 
 __all__ = ["RlkError", "lib", "logprob", "logprob_ws", "logprob_partials", "lse_merge",
            "consistency_stats", "workspace_size", "check_device_error", "vocab_tile", "row_tile",
+           "logprob_backward", "backward_workspace_size", "selected_token_logprob",
            "header_functions", "STAT_NAMES", "LIB_PATH", "HEADER_PATH"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +78,11 @@ def lib() -> ctypes.CDLL:
         L.rlk_check_device_error.argtypes = [P]
         L.rlk_shutdown.restype = st
         L.rlk_shutdown.argtypes = []
+        L.rlk_logprob_backward_workspace_size.restype = sz
+        L.rlk_logprob_backward_workspace_size.argtypes = [i64, i64, i64]
+        L.rlk_logprob_backward.restype = st
+        L.rlk_logprob_backward.argtypes = [P, P, P, P, P, i64, i64, i64, f32, P, P, ctypes.c_int,
+                                           P, sz, P]
         _lib = L
     return _lib
 
@@ -229,3 +235,73 @@ def consistency_stats(a, b, mask=None, stream=None):
 def check_device_error(stream=None):
     """Raise RlkError(RLK_ERR_TIMEOUT) if a device-side bounded wait ran out."""
     _check(lib().rlk_check_device_error(_stream(stream)), "rlk_check_device_error")
+
+
+def backward_workspace_size(T: int, H: int, V: int) -> int:
+    return lib().rlk_logprob_backward_workspace_size(int(T), int(H), int(V))
+
+
+def logprob_backward(h, W, targets, lse, grad_logp, inv_temp: float = 1.0, need_h: bool = True,
+                     need_W: bool = True, grad_W=None, workspace=None, stream=None):
+    """rlk_logprob_backward: returns (grad_h f32 [T,H] or None, grad_W f32 [V,H] or None,
+    workspace).  Pass grad_W to accumulate into it.  The workspace's first T*V*2 bytes
+    hold dz (bf16 [T,V]) afterwards."""
+    import torch
+    T, H, V = _check_inputs(h, W, targets)
+    _need(lse, torch.float32, "lse", 1)
+    _need(grad_logp, torch.float32, "grad_logp", 1)
+    gh = torch.empty((T, H), dtype=torch.float32, device=h.device) if need_h else None
+    accumulate = grad_W is not None
+    if need_W and grad_W is None:
+        grad_W = torch.empty((V, H), dtype=torch.float32, device=h.device)
+    if grad_W is not None:
+        _need(grad_W, torch.float32, "grad_W", 2)
+    if workspace is None:
+        workspace = torch.empty(backward_workspace_size(T, H, V), dtype=torch.uint8, device=h.device)
+    _need(workspace, torch.uint8, "workspace", 1)
+    _check(lib().rlk_logprob_backward(
+        _ptr(h), _ptr(W), _ptr(targets), _ptr(lse), _ptr(grad_logp), T, H, V,
+        ctypes.c_float(inv_temp), _ptr(gh) if gh is not None else None,
+        _ptr(grad_W) if (need_W or accumulate) else None, 1 if accumulate else 0,
+        _ptr(workspace), workspace.numel(), _stream(stream)), "rlk_logprob_backward")
+    return gh, (grad_W if (need_W or accumulate) else None), workspace
+
+
+def _autograd_function():
+    import torch
+
+    class SelectedTokenLogprob(torch.autograd.Function):
+        """logp = selected-token logprob; forward values from rlk_logprob (the
+        batch-invariant kernel), gradients from rlk_logprob_backward."""
+
+        @staticmethod
+        def forward(ctx, h, W, targets, inv_temp):
+            lp, lse, am = logprob(h, W, targets, inv_temp)
+            ctx.save_for_backward(h, W, targets, lse)
+            ctx.inv_temp = inv_temp
+            return lp
+
+        @staticmethod
+        def backward(ctx, grad_lp):
+            h, W, targets, lse = ctx.saved_tensors
+            need_h, need_W = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+            if not (need_h or need_W):
+                return None, None, None, None
+            gh, gW, _ = logprob_backward(h, W, targets, lse, grad_lp.contiguous().float(),
+                                         ctx.inv_temp, need_h=need_h, need_W=need_W)
+            return (gh.to(h.dtype) if need_h else None, gW.to(W.dtype) if need_W else None,
+                    None, None)
+
+    return SelectedTokenLogprob
+
+
+_SelectedTokenLogprob = None
+
+
+def selected_token_logprob(h, W, targets, inv_temp: float = 1.0):
+    """Differentiable selected-token logprob (torch autograd): the forward is the
+    batch-invariant kernel, the backward recomputes the logits on the same tiles."""
+    global _SelectedTokenLogprob
+    if _SelectedTokenLogprob is None:
+        _SelectedTokenLogprob = _autograd_function()
+    return _SelectedTokenLogprob.apply(h, W, targets, inv_temp)

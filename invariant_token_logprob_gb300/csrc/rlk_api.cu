@@ -144,10 +144,10 @@ size_t partial_bytes(int64_t T, int64_t V) {
     return size_t(T) * size_t(num_vocab_tiles(V)) * sizeof(rlk_partial);
 }
 
-// pad_buf: NULL, or (T < kMinTmaRows) room for kMinTmaRows zero-padded h rows.
-rlk_status launch_partials(const void* h, const void* W, const int32_t* tg, int64_t T,
-                           int64_t H, int64_t V, float inv_temp, void* partials, int num_sms,
-                           cudaStream_t stream, void* pad_buf = nullptr) {
+// Tensor maps of h and W for the LM-head kernel.  pad_buf: NULL, or (T <
+// kMinTmaRows) room for kMinTmaRows zero-padded h rows, filled here first.
+rlk_status prepare_maps(const void* h, const void* W, int64_t T, int64_t H, int64_t V,
+                        void* pad_buf, cudaStream_t stream, CUtensorMap* th, CUtensorMap* tw) {
     int64_t h_rows = T;
     if (pad_buf) {
         cudaError_t e = rlk::launch_pad_rows(h, T, H, pad_buf, stream);
@@ -155,10 +155,17 @@ rlk_status launch_partials(const void* h, const void* W, const int32_t* tg, int6
         h = pad_buf;
         h_rows = rlk::kMinTmaRows;
     }
-    CUtensorMap th, tw;
-    if (!encode_bf16_2d(&th, h, h_rows, H, kRowTile) ||
-        !encode_bf16_2d(&tw, W, V, H, kVocabTile))
+    if (!encode_bf16_2d(th, h, h_rows, H, kRowTile) || !encode_bf16_2d(tw, W, V, H, kVocabTile))
         return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status launch_partials(const void* h, const void* W, const int32_t* tg, int64_t T,
+                           int64_t H, int64_t V, float inv_temp, void* partials, int num_sms,
+                           cudaStream_t stream, void* pad_buf = nullptr) {
+    CUtensorMap th, tw;
+    rlk_status st = prepare_maps(h, W, T, H, V, pad_buf, stream, &th, &tw);
+    if (st != RLK_OK) return st;
     return from_cuda(rlk::launch_lmhead_partials(&th, &tw, tg, partials, T, V, H, inv_temp,
                                                  num_sms, stream));
 }
@@ -293,6 +300,46 @@ rlk_status rlk_logprob(const void* hidden_bf16, const void* weight_bf16,
                                            out_argmax_i32, s));
 }
 
+size_t rlk_logprob_backward_workspace_size(int64_t T, int64_t H, int64_t V) {
+    if (T <= 0 || V <= 0 || H <= 0) return 0;
+    size_t bytes = (size_t(T) * size_t(V) * 2 + 15) / 16 * 16;
+    if (T < rlk::kMinTmaRows) bytes += size_t(rlk::kMinTmaRows) * size_t(H) * 2;
+    return bytes;
+}
+
+rlk_status rlk_logprob_backward(const void* hidden_bf16, const void* weight_bf16,
+                                const int32_t* targets_i32, const float* lse_f32,
+                                const float* grad_logp_f32, int64_t T, int64_t H, int64_t V,
+                                float inv_temp, float* grad_hidden_f32, float* grad_weight_f32,
+                                int accumulate_grad_weight, void* workspace,
+                                size_t workspace_bytes, rlk_stream_t stream) {
+    rlk_status st = check_shape(T, H, V, inv_temp);
+    if (st != RLK_OK) return st;
+    if (T == 0) return RLK_OK;
+    if ((st = check_operands(hidden_bf16, weight_bf16, targets_i32, H)) != RLK_OK) return st;
+    if (!lse_f32 || !grad_logp_f32) return RLK_ERR_INVALID_ARG;
+    if (!aligned4(lse_f32) || !aligned4(grad_logp_f32) || !aligned4(grad_hidden_f32) ||
+        !aligned4(grad_weight_f32))
+        return RLK_ERR_ALIGNMENT;
+    if (!workspace) return RLK_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return RLK_ERR_ALIGNMENT;
+    if (workspace_bytes < rlk_logprob_backward_workspace_size(T, H, V)) return RLK_ERR_WORKSPACE;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t dz_bytes = (size_t(T) * size_t(V) * 2 + 15) / 16 * 16;
+    void* pad = T < rlk::kMinTmaRows ? static_cast<char*>(workspace) + dz_bytes : nullptr;
+    CUtensorMap th, tw;
+    if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, pad, s, &th, &tw)) != RLK_OK)
+        return st;
+    cudaError_t e = rlk::launch_lmhead_grad_logits(&th, &tw, targets_i32, lse_f32, grad_logp_f32,
+                                                   workspace, T, V, H, inv_temp, sms, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    e = rlk::run_backward_gemms(hidden_bf16, weight_bf16, workspace, T, H, V, inv_temp,
+                                grad_hidden_f32, grad_weight_f32, accumulate_grad_weight != 0, s);
+    return from_cuda(e);
+}
+
 rlk_status rlk_consistency_stats(const float* logp_a, const float* logp_b, const int8_t* mask,
                                  int64_t n, double* out, rlk_stream_t stream) {
     if (!out || n < 0) return RLK_ERR_INVALID_ARG;
@@ -335,6 +382,7 @@ rlk_status rlk_shutdown(void) {
     }
     g_ws.clear();
     if (have_prev) cudaSetDevice(prev);
+    rlk::release_backward_handles();
     return st;
 }
 

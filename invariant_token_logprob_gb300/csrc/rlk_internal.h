@@ -27,6 +27,21 @@ cudaError_t launch_lmhead_partials(const CUtensorMap* th, const CUtensorMap* tw,
                                    const int32_t* targets, void* partials, int64_t T, int64_t V,
                                    int64_t H, float inv_temp, int num_sms, cudaStream_t stream);
 
+// Same main loop with the backward epilogue: recomputes the logits and writes
+// dz[t][v] = grad[t] * ([v == target[t]] - exp(z[t][v] - lse[t])) as bf16
+// (0 for rows whose target lies outside [0, V)); dz is [T][V] row-major.
+cudaError_t launch_lmhead_grad_logits(const CUtensorMap* th, const CUtensorMap* tw,
+                                      const int32_t* targets, const float* lse, const float* grad,
+                                      void* dz, int64_t T, int64_t V, int64_t H, float inv_temp,
+                                      int num_sms, cudaStream_t stream);
+
+// grad_h [T][H] = inv_temp * dz . W and grad_W [V][H] (+)= inv_temp * dz^T . h
+// with fp32 accumulation (library GEMMs; either output may be null).
+cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, int64_t T,
+                               int64_t H, int64_t V, float inv_temp, float* grad_h,
+                               float* grad_W, bool accumulate_W, cudaStream_t stream);
+void release_backward_handles();
+
 // Reads and clears the per-device error word of the LM-head kernel (bit 0: a
 // bounded wait ran out).  Synchronous on the current device.
 cudaError_t lmhead_take_error(unsigned int* out);

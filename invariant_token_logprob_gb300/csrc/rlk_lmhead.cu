@@ -28,6 +28,7 @@
 //               row, warp w reads TMEM lanes 32*(w%4) .. +31
 // The accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue
 // of tile i overlaps the MMAs of tile i+1.  Every wait is bounded in time.
+#include <cuda_bf16.h>
 #include <limits.h>
 
 #include "rlk_internal.h"
@@ -63,7 +64,10 @@ __device__ unsigned int g_lmhead_error;
 
 struct Args {
     const int32_t* targets;
-    float4* partials;
+    float4* partials;      // mode 0: [T][num_n] records
+    const float* lse;      // mode 1: forward LSE per row
+    const float* grad;     // mode 1: upstream gradient of logp per row
+    uint16_t* dz;          // mode 1: [T][V] bf16 gradient of logp w.r.t. the logits
     int64_t T;
     int V;
     int num_m;   // row tiles
@@ -118,9 +122,20 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
     }
 }
 
+// Epilogue modes of the one kernel: the main loop is shared, so the logits a
+// mode sees are the same fp32 values in both.
+constexpr int kModePartials = 0;   // forward: vocabulary-tile partial records
+constexpr int kModeGradLogits = 1; // backward: dz = g (onehot - exp(z - lse)) as bf16
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
-    lmhead_partials_kernel(const __grid_constant__ CUtensorMap tmap_h,
-                           const __grid_constant__ CUtensorMap tmap_w, const Args p) {
+    lmhead_kernel(const __grid_constant__ CUtensorMap tmap_h,
+                  const __grid_constant__ CUtensorMap tmap_w, const Args p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -260,53 +275,103 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
 
-            const int col0 = n * kBN;
-            const int ncols = min(kBN, p.V - col0);
-            const int nchunks = (ncols + 31) >> 5;
-            float run_m = -INFINITY, run_s = 0.0f, zt = 0.0f;
-            int32_t run_a = INT_MAX;
-            const uint32_t t_addr = lane_base + acc * uint32_t(kBN);
-            for (int c = 0; c < nchunks; ++c) {
-                uint32_t r[32];
-                tmem_ld32(t_addr + uint32_t(c * 32), r);
-                tmem_ld_wait();
-                float z[32];
+            if constexpr (kMode == kModePartials) {
+                const int col0 = n * kBN;
+                const int ncols = min(kBN, p.V - col0);
+                const int nchunks = (ncols + 31) >> 5;
+                float run_m = -INFINITY, run_s = 0.0f, zt = 0.0f;
+                int32_t run_a = INT_MAX;
+                const uint32_t t_addr = lane_base + acc * uint32_t(kBN);
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_addr + uint32_t(c * 32), r);
+                    tmem_ld_wait();
+                    float z[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r[j]) * inv_temp;
-                const int nvalid = ncols - c * 32;
-                if (nvalid < 32) {
+                    for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r[j]) * inv_temp;
+                    const int nvalid = ncols - c * 32;
+                    if (nvalid < 32) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j >= nvalid) z[j] = -INFINITY;  // columns past V
-                }
-                float cm = z[0];
-                int ca = 0;
-#pragma unroll
-                for (int j = 1; j < 32; ++j)
-                    if (z[j] > cm) {
-                        cm = z[j];
-                        ca = j;
+                        for (int j = 0; j < 32; ++j)
+                            if (j >= nvalid) z[j] = -INFINITY;  // columns past V
                     }
-                const float cml = cm * kLog2e;
-                float cs = 0.0f;
+                    float cm = z[0];
+                    int ca = 0;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) cs += exp2f(fmaf(z[j], kLog2e, -cml));
-                const int cbase = col0 + c * 32;
-                const int rel = tgt - cbase;
-                if (unsigned(rel) < 32u) {
+                    for (int j = 1; j < 32; ++j)
+                        if (z[j] > cm) {
+                            cm = z[j];
+                            ca = j;
+                        }
+                    const float cml = cm * kLog2e;
+                    float cs = 0.0f;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j == rel) zt = z[j];
+                    for (int j = 0; j < 32; ++j) cs += exp2f(fmaf(z[j], kLog2e, -cml));
+                    const int cbase = col0 + c * 32;
+                    const int rel = tgt - cbase;
+                    if (unsigned(rel) < 32u) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j == rel) zt = z[j];
+                    }
+                    lse_combine(run_m, run_s, run_a, cm, cs, cbase + ca);
                 }
-                lse_combine(run_m, run_s, run_a, cm, cs, cbase + ca);
+                // Accumulator buffer fully read: hand it back to the MMA warp.
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                if (row < p.T)
+                    p.partials[row * p.num_n + n] =
+                        make_float4(run_m, run_s, __int_as_float(run_a), zt);
+            } else {
+                const int col0 = n * kBN;
+                const int ncols = min(kBN, p.V - col0);
+                const int nchunks = (ncols + 31) >> 5;
+                const uint32_t t_addr = lane_base + acc * uint32_t(kBN);
+                const bool live = row < p.T;
+                const bool valid = live && tgt >= 0 && tgt < p.V;
+                const float g = valid ? __ldg(p.grad + row) : 0.0f;
+                const float lse2 = live ? __ldg(p.lse + row) * kLog2e : 0.0f;
+                uint16_t* dz_row = p.dz + (live ? row : 0) * int64_t(p.V);
+                const bool vec_ok = (p.V & 7) == 0;  // rows start on 16-byte boundaries
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_addr + uint32_t(c * 32), r);
+                    tmem_ld_wait();
+                    const int cbase = col0 + c * 32;
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const float z0 = __uint_as_float(r[j]) * inv_temp;
+                        const float z1 = __uint_as_float(r[j + 1]) * inv_temp;
+                        // p = exp(z - lse); dz = g * (onehot - p)
+                        const float p0 = exp2f(fmaf(z0, kLog2e, -lse2));
+                        const float p1 = exp2f(fmaf(z1, kLog2e, -lse2));
+                        const float d0 = valid ? g * ((cbase + j == tgt ? 1.0f : 0.0f) - p0) : 0.0f;
+                        const float d1 =
+                            valid ? g * ((cbase + j + 1 == tgt ? 1.0f : 0.0f) - p1) : 0.0f;
+                        packed[j / 2] = pack_bf16x2(d0, d1);
+                    }
+                    const int nvalid = ncols - c * 32;
+                    if (live && nvalid >= 32 && vec_ok) {
+                        uint4* dst = reinterpret_cast<uint4*>(dz_row + cbase);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            dst[q4] = make_uint4(packed[4 * q4], packed[4 * q4 + 1],
+                                                 packed[4 * q4 + 2], packed[4 * q4 + 3]);
+                    } else if (live) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nvalid)
+                                dz_row[cbase + j] =
+                                    uint16_t((packed[j / 2] >> (16 * (j & 1))) & 0xFFFFu);
+                    }
+                    __syncwarp();  // reconverge before the next warp-wide TMEM load
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
             }
-            // Accumulator buffer fully read: hand it back to the MMA warp.
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
-            if (row < p.T)
-                p.partials[row * p.num_n + n] =
-                    make_float4(run_m, run_s, __int_as_float(run_a), zt);
             if (++acc == kAccBufs) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -322,36 +387,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-int g_configured[64];  // per device: dynamic shared memory attribute set
+int g_configured[2][64];  // per mode and device: dynamic shared memory attribute set
+
+template <int kMode>
+cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, int64_t H,
+                        int num_sms, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && !g_configured[kMode][dev]) {
+        e = cudaFuncSetAttribute(lmhead_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        g_configured[kMode][dev] = 1;
+    }
+    a.num_m = int((a.T + kBM - 1) / kBM);
+    a.num_n = int((a.V + kBN - 1) / kBN);
+    a.num_kb = int((H + kBK - 1) / kBK);
+    a.band = a.num_m < 32 ? a.num_m : 32;
+    a.num_tiles = a.num_m * a.num_n;
+    const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
+    lmhead_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(*th, *tw, a);
+    return cudaGetLastError();
+}
 
 }  // namespace
 
 cudaError_t launch_lmhead_partials(const CUtensorMap* th, const CUtensorMap* tw,
                                    const int32_t* targets, void* partials, int64_t T, int64_t V,
                                    int64_t H, float inv_temp, int num_sms, cudaStream_t stream) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && !g_configured[dev]) {
-        e = cudaFuncSetAttribute(lmhead_partials_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(kSmemBytes));
-        if (e != cudaSuccess) return e;
-        g_configured[dev] = 1;
-    }
-    Args a;
+    Args a = {};
     a.targets = targets;
     a.partials = static_cast<float4*>(partials);
     a.T = T;
     a.V = int(V);
-    a.num_m = int((T + kBM - 1) / kBM);
-    a.num_n = int((V + kBN - 1) / kBN);
-    a.num_kb = int((H + kBK - 1) / kBK);
-    a.band = a.num_m < 32 ? a.num_m : 32;
-    a.num_tiles = a.num_m * a.num_n;
     a.inv_temp = inv_temp;
-    const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
-    lmhead_partials_kernel<<<grid, kThreads, kSmemBytes, stream>>>(*th, *tw, a);
-    return cudaGetLastError();
+    return launch_mode<kModePartials>(th, tw, a, H, num_sms, stream);
+}
+
+cudaError_t launch_lmhead_grad_logits(const CUtensorMap* th, const CUtensorMap* tw,
+                                      const int32_t* targets, const float* lse, const float* grad,
+                                      void* dz, int64_t T, int64_t V, int64_t H, float inv_temp,
+                                      int num_sms, cudaStream_t stream) {
+    Args a = {};
+    a.targets = targets;
+    a.lse = lse;
+    a.grad = grad;
+    a.dz = static_cast<uint16_t*>(dz);
+    a.T = T;
+    a.V = int(V);
+    a.inv_temp = inv_temp;
+    return launch_mode<kModeGradLogits>(th, tw, a, H, num_sms, stream);
 }
 
 cudaError_t lmhead_take_error(unsigned int* out) {

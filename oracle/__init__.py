@@ -51,6 +51,10 @@ def _bind(lib):
     lib.oracle_merge_blocks.argtypes = [P, P, P, P, P, i64, i64, i64, i64, P, P, P]
     lib.oracle_consistency_stats.restype = ctypes.c_int
     lib.oracle_consistency_stats.argtypes = [P, P, P, i64, P]
+    lib.oracle_logprob_backward.restype = ctypes.c_int
+    lib.oracle_logprob_backward.argtypes = [P, P, P, P, i64, i64, i64, ctypes.c_float, P, P, P]
+    lib.oracle_logprob_f64.restype = ctypes.c_int
+    lib.oracle_logprob_f64.argtypes = [P, P, P, i64, i64, i64, ctypes.c_double, P, P]
     return lib
 
 
@@ -182,4 +186,40 @@ def consistency_stats(a, b, mask=None, lib=None) -> np.ndarray:
     rc = lib.oracle_consistency_stats(_ptr(a), _ptr(b), _ptr(mk), a.shape[0], _ptr(out))
     if rc != 0:
         raise ValueError("oracle_consistency_stats rejected its arguments")
+    return out
+
+
+def logprob_backward(h, W, targets, grad, inv_temp: float = 1.0, lib=None) -> dict:
+    """fp64 gradients of logp w.r.t. the logits, h and W: dict(dz [T,V], dh [T,H],
+    dW [V,H]) for upstream gradient `grad` [T] (small problems only)."""
+    lib = lib or load()
+    h = _u16(h)
+    W = _u16(W)
+    tg = _i32(targets)
+    g = np.ascontiguousarray(np.asarray(grad.detach().cpu().numpy() if hasattr(grad, "detach")
+                                        else grad, dtype=np.float64))
+    T, H = h.shape
+    V = W.shape[0]
+    out = {"dz": np.zeros((T, V)), "dh": np.zeros((T, H)), "dW": np.zeros((V, H))}
+    rc = lib.oracle_logprob_backward(_ptr(h), _ptr(W), _ptr(tg), _ptr(g), T, H, V,
+                                     ctypes.c_float(inv_temp), _ptr(out["dz"]), _ptr(out["dh"]),
+                                     _ptr(out["dW"]))
+    if rc != 0:
+        raise ValueError("oracle_logprob_backward rejected its arguments")
+    return out
+
+
+def logprob_f64(h, W, targets, inv_temp: float = 1.0, lib=None) -> dict:
+    """Forward on fp64 inputs (h [T,H], W [V,H] float64): dict(logp, lse)."""
+    lib = lib or load()
+    h = np.ascontiguousarray(h, dtype=np.float64)
+    W = np.ascontiguousarray(W, dtype=np.float64)
+    tg = _i32(targets)
+    T, H = h.shape
+    V = W.shape[0]
+    out = {"logp": np.zeros(T), "lse": np.zeros(T)}
+    rc = lib.oracle_logprob_f64(_ptr(h), _ptr(W), _ptr(tg), T, H, V, float(inv_temp),
+                                _ptr(out["logp"]), _ptr(out["lse"]))
+    if rc != 0:
+        raise ValueError("oracle_logprob_f64 rejected its arguments")
     return out

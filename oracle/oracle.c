@@ -362,3 +362,113 @@ int oracle_consistency_stats(const float *a, const float *b, const int8_t *mask,
     out[7] = (double)first;
     return 0;
 }
+
+
+/* ------------------------------------------------------------------------
+ * Backward of the selected-token logprob (the training half of the method:
+ * "Finish RL Training Faster ...", section "核心设计范式：推理算子定义数值基准，
+ * 训练仅挂接反向求导" -- the forward values come from the inference kernel, the
+ * training side supplies the derivative through a custom autograd function).
+ * With p = softmax(z) and upstream gradient g[t] of logp[t]:
+ *   dz[t,v] = g[t] * ([v == target[t]] - p[t,v])      (0 for an ignored row)
+ *   dh[t,k] = inv_temp * sum_v dz[t,v] W[v,k]
+ *   dW[v,k] = inv_temp * sum_t dz[t,v] h[t,k]
+ * (z = inv_temp * h.W^T, so dlogp/dh and dlogp/dW carry one inv_temp factor.)
+ * Computed by definition in fp64: logits and LSE as in oracle_logprob, p by
+ * exp(z - LSE), sums in index order.  Small problems only (T*V*H work).
+ * Outputs: dz [T][V], dh [T][H], dW [V][H] (any may be NULL).
+ */
+static void logits_all(const double *hd, const double *Wd, int64_t H, int64_t V,
+                       double it, double *z)
+{
+    for (int64_t v = 0; v < V; ++v) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < H; ++k)
+            acc += hd[k] * Wd[v * H + k];
+        z[v] = acc * it;
+    }
+}
+
+static int backward_core(const double *hd, const double *Wd, const int32_t *targets,
+                         const double *grad, int64_t T, int64_t H, int64_t V, double it,
+                         double *out_dz, double *out_dh, double *out_dW)
+{
+    double *z = (double *)malloc((size_t)V * sizeof(double));
+    double *dz = (double *)malloc((size_t)T * (size_t)V * sizeof(double));
+    if (!z || !dz) { free(z); free(dz); return -1; }
+    for (int64_t t = 0; t < T; ++t) {
+        logits_all(hd + t * H, Wd, H, V, it, z);
+        row_result r = logprob_row(z, V, targets[t]);
+        int32_t tg = targets[t];
+        int valid = tg >= 0 && (int64_t)tg < V;
+        for (int64_t v = 0; v < V; ++v) {
+#if ORACLE_MUTANT == 9
+            double p = exp(z[v] - r.zmax);       /* mutant: unnormalised softmax */
+#else
+            double p = exp(z[v] - r.lse);
+#endif
+            dz[t * V + v] = valid ? grad[t] * ((v == tg ? 1.0 : 0.0) - p) : 0.0;
+        }
+    }
+    if (out_dz) memcpy(out_dz, dz, (size_t)T * (size_t)V * sizeof(double));
+    if (out_dh)
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t k = 0; k < H; ++k) {
+                double acc = 0.0;
+                for (int64_t v = 0; v < V; ++v)
+                    acc += dz[t * V + v] * Wd[v * H + k];
+#if ORACLE_MUTANT == 8
+                out_dh[t * H + k] = acc;         /* mutant: drops the inv_temp factor */
+#else
+                out_dh[t * H + k] = it * acc;
+#endif
+            }
+    if (out_dW)
+        for (int64_t v = 0; v < V; ++v)
+            for (int64_t k = 0; k < H; ++k) {
+                double acc = 0.0;
+                for (int64_t t = 0; t < T; ++t)
+                    acc += dz[t * V + v] * hd[t * H + k];
+                out_dW[v * H + k] = it * acc;
+            }
+    free(z);
+    free(dz);
+    return 0;
+}
+
+int oracle_logprob_backward(const uint16_t *h, const uint16_t *W, const int32_t *targets,
+                            const double *grad, int64_t T, int64_t H, int64_t V, float inv_temp,
+                            double *out_dz, double *out_dh, double *out_dW)
+{
+    if (!h || !W || !targets || !grad || T < 1 || H < 1 || V < 1)
+        return -1;
+    double *hd = (double *)malloc((size_t)T * (size_t)H * sizeof(double));
+    double *Wd = (double *)malloc((size_t)V * (size_t)H * sizeof(double));
+    if (!hd || !Wd) { free(hd); free(Wd); return -1; }
+    for (int64_t i = 0; i < T * H; ++i) hd[i] = bf16_to_double(h[i]);
+    for (int64_t i = 0; i < V * H; ++i) Wd[i] = bf16_to_double(W[i]);
+    int rc = backward_core(hd, Wd, targets, grad, T, H, V, (double)inv_temp, out_dz, out_dh,
+                           out_dW);
+    free(hd);
+    free(Wd);
+    return rc;
+}
+
+/* Forward on fp64 inputs (used to pin the backward by finite differences:
+ * the oracle's own logp, perturbed input by input). */
+int oracle_logprob_f64(const double *h, const double *W, const int32_t *targets, int64_t T,
+                       int64_t H, int64_t V, double inv_temp, double *out_logp, double *out_lse)
+{
+    if (!h || !W || !targets || T < 1 || H < 1 || V < 1)
+        return -1;
+    double *z = (double *)malloc((size_t)V * sizeof(double));
+    if (!z) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        logits_all(h + t * H, W, H, V, inv_temp, z);
+        row_result r = logprob_row(z, V, targets[t]);
+        if (out_logp) out_logp[t] = r.logp;
+        if (out_lse) out_lse[t] = r.lse;
+    }
+    free(z);
+    return 0;
+}

@@ -281,9 +281,71 @@ def _bf16_bits_round(x: np.ndarray) -> np.ndarray:
     return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
 
 
+def pin_backward_finite_differences(lib):
+    """dh and dW of the oracle backward equal central finite differences of the
+    oracle's own fp64 forward (loss = sum_t g_t logp_t), with inv_temp != 1 and
+    an ignored row."""
+    rng = np.random.default_rng(21)
+    T, H, V, it = 3, 5, 11, 1.5
+    hb = _bf16_bits_round(rng.standard_normal((T, H)).astype(np.float32))
+    Wb = _bf16_bits_round((0.7 * rng.standard_normal((V, H))).astype(np.float32))
+    hf, Wf = _bits_to_f64(hb), _bits_to_f64(Wb)
+    tg = np.array([4, -1, 10], np.int32)
+    g = np.array([0.7, 1.3, -0.4])
+    b = oracle.logprob_backward(hb, Wb, tg, g, it, lib=lib)
+
+    def loss(hh, WW):
+        return float(np.dot(g, oracle.logprob_f64(hh, WW, tg, it, lib=lib)["logp"]))
+
+    eps = 1e-6
+    for t in range(T):
+        for k in range(H):
+            hp, hm = hf.copy(), hf.copy()
+            hp[t, k] += eps
+            hm[t, k] -= eps
+            fd = (loss(hp, Wf) - loss(hm, Wf)) / (2 * eps)
+            assert abs(b["dh"][t, k] - fd) <= 1e-6 * max(1.0, abs(fd)), (t, k, b["dh"][t, k], fd)
+    for v in range(V):
+        for k in range(H):
+            Wp, Wm = Wf.copy(), Wf.copy()
+            Wp[v, k] += eps
+            Wm[v, k] -= eps
+            fd = (loss(hf, Wp) - loss(hf, Wm)) / (2 * eps)
+            assert abs(b["dW"][v, k] - fd) <= 1e-6 * max(1.0, abs(fd)), (v, k, b["dW"][v, k], fd)
+    # dz sums to zero over the vocabulary on valid rows and is 0 on ignored rows
+    assert np.allclose(b["dz"].sum(1)[[0, 2]], 0.0, atol=1e-14)
+    assert np.all(b["dz"][1] == 0.0) and np.all(b["dh"][1] == 0.0)
+
+
+def pin_backward_closed_forms(lib):
+    """W = 0: p is uniform, so dz = g (onehot - 1/V), dh = 0 and
+    dW[v] = inv_temp sum_t g_t (onehot_v - 1/V) h_t.  Temperature: (inv_temp 2, W)
+    and (1, 2W) give the same dh, and dW halves."""
+    rng = np.random.default_rng(22)
+    T, H, V = 4, 6, 9
+    hb = _bf16_bits_round(rng.standard_normal((T, H)).astype(np.float32))
+    hf = _bits_to_f64(hb)
+    tg = rng.integers(0, V, T).astype(np.int32)
+    g = rng.standard_normal(T)
+    b = oracle.logprob_backward(hb, np.zeros((V, H), np.uint16), tg, g, 2.0, lib=lib)
+    onehot = np.zeros((T, V))
+    onehot[np.arange(T), tg] = 1.0
+    dz = g[:, None] * (onehot - 1.0 / V)
+    assert np.allclose(b["dz"], dz, atol=1e-15)
+    assert np.all(b["dh"] == 0.0)
+    assert np.allclose(b["dW"], 2.0 * dz.T @ hf, atol=1e-13)
+    Wb = _bf16_bits_round((0.3 * rng.standard_normal((V, H))).astype(np.float32))
+    W2 = _bf16_bits((2.0 * _bits_to_f64(Wb)).astype(np.float32))
+    a = oracle.logprob_backward(hb, Wb, tg, g, 2.0, lib=lib)
+    c = oracle.logprob_backward(hb, W2, tg, g, 1.0, lib=lib)
+    assert np.allclose(a["dh"], c["dh"], rtol=1e-13, atol=1e-15)
+    assert np.allclose(a["dW"], 2.0 * c["dW"], rtol=1e-13, atol=1e-15)
+
+
 PINS = [pin_zero_weights, pin_one_hot_dominant, pin_shift_invariance, pin_temperature,
         pin_brute_force_exact, pin_scipy_logsumexp, pin_ignored_targets,
-        pin_block_stats_and_merge, pin_worked_example, pin_stats_closed_forms]
+        pin_block_stats_and_merge, pin_worked_example, pin_stats_closed_forms,
+        pin_backward_finite_differences, pin_backward_closed_forms]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -310,10 +372,11 @@ def test_tie_rows_of_tiny_input(olib):
 
 
 def test_pins_catch_planted_mistakes(tmp_path):
-    """Each deliberate mistake of oracle.c (ORACLE_MUTANT 1..7: dropped term,
+    """Each deliberate mistake of oracle.c (ORACLE_MUTANT 1..9: dropped term,
     divided temperature, highest-index ties, LSE without the max, flipped logp
-    sign, swapped gap direction, sample variance) fails at least one pin."""
-    for mutant in range(1, 8):
+    sign, swapped gap direction, sample variance, backward without inv_temp,
+    unnormalised softmax in the backward) fails at least one pin."""
+    for mutant in range(1, 10):
         path = str(tmp_path / f"liboracle_m{mutant}.so")
         oracle.build(path, mutant=mutant)
         lib = oracle.load(path)
