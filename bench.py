@@ -19,7 +19,8 @@ e2e tokens/s through rlk_logprob with pinned host buffers (H2D of h and
 targets, D2H of logp/lse/argmax inside the timed region; W stays resident as
 model weights do), the dominant kernel's roofline from live CUDA events, SM
 clocks sampled during the timed region, the CPU oracle's throughput on a
-bounded sample, and decode-regime points (T = 1, 16: HBM-bound).
+bounded sample, decode-regime points (T = 1..16: HBM-bound) and the backward
+(rlk_logprob_backward on the same batch).
 
 --impl reference times the fp64 CPU oracle (the only reference this method
 has) on the host cores, each step a bounded sample of the same workload.
@@ -55,6 +56,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-backward", action="store_true")
     p.add_argument("--decode-only", action="store_true",
                    help="time only the decode regime at T = --decode-T (for profiling)")
     p.add_argument("--decode-T", type=int, default=1)
@@ -287,6 +289,45 @@ def decode_points(rlk, torch, W, stream, pk, Ts=(1, 2, 4, 8, 16), reps=50, round
     return res
 
 
+def backward_point(rlk, torch, h, W, tg, pk, reps=10):
+    """Backward of the same workload (T=4096): rlk_logprob_backward producing both
+    fp32 gradients (recompute GEMM + dz epilogue, then the two library GEMMs),
+    and the fused recompute/dz kernel alone (both outputs NULL)."""
+    T, H = h.shape
+    V = W.shape[0]
+    lp, lse, am = rlk.logprob(h, W, tg, 1.0)
+    grad = torch.ones(T, device=h.device)
+    ws = torch.empty(rlk.backward_workspace_size(T, H, V), dtype=torch.uint8, device=h.device)
+    gW = torch.empty((V, H), dtype=torch.float32, device=h.device)
+    stream = torch.cuda.current_stream()
+
+    def timed(need_h, need_W):
+        for _ in range(2):
+            rlk.logprob_backward(h, W, tg, lse, grad, 1.0, need_h=need_h, need_W=need_W,
+                                 workspace=ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            rlk.logprob_backward(h, W, tg, lse, grad, 1.0, need_h=need_h, need_W=need_W,
+                                 workspace=ws)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e-3
+
+    t_all = timed(True, True)
+    t_dz = timed(False, False)
+    rlk.check_device_error()
+    gemm = 2.0 * T * H * V
+    del gW
+    return dict(tokens_per_s=T / t_all, ms_per_call=t_all * 1e3,
+                tflops=3 * gemm / t_all / 1e12, frac=3 * gemm / t_all / 1e12 / pk["bf16_tflops"],
+                grad_logits_kernel_ms=t_dz * 1e3,
+                grad_logits_kernel_frac=gemm / t_dz / 1e12 / pk["bf16_tflops"],
+                gemms_ms=(t_all - t_dz) * 1e3,
+                note="flops = 3 x 2*T*H*V (recompute, dz.W, dz^T.h); peak = bf16 burst")
+
+
 def run_decode_only(args):
     """Decode regime alone (T = --decode-T rows per call, H=4096, V=151936): used
     for profiling the weight-streaming regime; prints one JSON line."""
@@ -404,6 +445,9 @@ def run_ours(args):
     decode = None
     if not args.no_decode:
         decode = decode_points(rlk, torch, W, stream, pk)
+    backward = None
+    if not args.no_backward:
+        backward = backward_point(rlk, torch, h, W, tg, pk)
 
     if rank != 0:
         return 0
@@ -413,6 +457,7 @@ def run_ours(args):
     tr = recorded_traffic()
     roofline = dict(bound="tensor", achieved=achieved, peak=pk["bf16_tflops"], unit="TFLOP/s",
                     frac=achieved / pk["bf16_tflops"],
+                    frac_of_sustained=achieved / pk["bf16_tflops_sustained"],
                     peak_source=f"bf16_tflops burst, {pk['source']} (MEASURED_PEAKS.json)"
                     if pk["source"] == "measured" else "fallback 1.9 PFLOP/s",
                     traffic=(tr["bytes_per_launch"] if tr else None),
@@ -436,7 +481,7 @@ def run_ours(args):
                 clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"],
                             reasons=clk["reasons"], samples=clk["samples"],
                             window=clk.get("window")),
-                decode=decode, bitwise_mismatch_vs_first_call=mism)
+                decode=decode, backward=backward, bitwise_mismatch_vs_first_call=mism)
     print(json.dumps(line), flush=True)
     return 0
 

@@ -161,6 +161,25 @@ rlk_status rlk_lse_merge(const rlk_partial *partials, const int32_t *targets_i32
                          int32_t *out_argmax_i32, rlk_stream_t stream);
 
 /*
+ * rlk_logprob plus the per-token entropy of the softmax over the whole
+ * vocabulary, entropy[t] = -sum_v p[t][v] log p[t][v] (the actor-entropy signal
+ * reported next to rewards in "Finish RL Training Faster: Bitwise-Consistent,
+ * High-Performance, Agent-Driven", Nemotron results).  Each vocabulary tile
+ * also keeps u = sum exp(z - m)(z - m) about its own max m; the fixed-tree merge
+ * folds u alongside (m, s) and writes entropy = log S - U / S.  The logp, lse
+ * and argmax written here are bit-identical to rlk_logprob's.
+ *   out_entropy_f32  device [T] float
+ *   workspace        device, 16-byte aligned, >= rlk_logprob_entropy_workspace_size
+ * Other arguments as rlk_logprob_ws.  Allocates nothing; asynchronous.
+ */
+size_t rlk_logprob_entropy_workspace_size(int64_t T, int64_t H, int64_t V);
+rlk_status rlk_logprob_entropy(const void *hidden_bf16, const void *weight_bf16,
+                               const int32_t *targets_i32, int64_t T, int64_t H, int64_t V,
+                               float inv_temp, float *out_logp_f32, float *out_lse_f32,
+                               int32_t *out_argmax_i32, float *out_entropy_f32, void *workspace,
+                               size_t workspace_bytes, rlk_stream_t stream);
+
+/*
  * Backward of the selected-token logprob (the training half of the method:
  * "Finish RL Training Faster: Bitwise-Consistent, High-Performance,
  * Agent-Driven", section "核心设计范式：推理算子定义数值基准，训练仅挂接反向求导" --

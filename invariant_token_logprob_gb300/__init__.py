@@ -19,6 +19,7 @@ from typing import Optional
 __all__ = ["RlkError", "lib", "logprob", "logprob_ws", "logprob_partials", "lse_merge",
            "consistency_stats", "workspace_size", "check_device_error", "vocab_tile", "row_tile",
            "logprob_backward", "backward_workspace_size", "selected_token_logprob",
+           "logprob_entropy", "entropy_workspace_size",
            "header_functions", "STAT_NAMES", "LIB_PATH", "HEADER_PATH"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -78,6 +79,10 @@ def lib() -> ctypes.CDLL:
         L.rlk_check_device_error.argtypes = [P]
         L.rlk_shutdown.restype = st
         L.rlk_shutdown.argtypes = []
+        L.rlk_logprob_entropy_workspace_size.restype = sz
+        L.rlk_logprob_entropy_workspace_size.argtypes = [i64, i64, i64]
+        L.rlk_logprob_entropy.restype = st
+        L.rlk_logprob_entropy.argtypes = [P, P, P, i64, i64, i64, f32, P, P, P, P, P, sz, P]
         L.rlk_logprob_backward_workspace_size.restype = sz
         L.rlk_logprob_backward_workspace_size.argtypes = [i64, i64, i64]
         L.rlk_logprob_backward.restype = st
@@ -305,3 +310,24 @@ def selected_token_logprob(h, W, targets, inv_temp: float = 1.0):
     if _SelectedTokenLogprob is None:
         _SelectedTokenLogprob = _autograd_function()
     return _SelectedTokenLogprob.apply(h, W, targets, inv_temp)
+
+
+def entropy_workspace_size(T: int, H: int, V: int) -> int:
+    return lib().rlk_logprob_entropy_workspace_size(int(T), int(H), int(V))
+
+
+def logprob_entropy(h, W, targets, inv_temp: float = 1.0, workspace=None, stream=None):
+    """rlk_logprob_entropy: returns (logp, lse, argmax, entropy)."""
+    import torch
+    T, H, V = _check_inputs(h, W, targets)
+    lp, lse, am = _outputs(T, h.device, None)
+    ent = torch.empty(T, dtype=torch.float32, device=h.device)
+    if workspace is None:
+        workspace = torch.empty(max(1, entropy_workspace_size(T, H, V)), dtype=torch.uint8,
+                                device=h.device)
+    _need(workspace, torch.uint8, "workspace", 1)
+    _check(lib().rlk_logprob_entropy(_ptr(h), _ptr(W), _ptr(targets), T, H, V,
+                                     ctypes.c_float(inv_temp), _ptr(lp), _ptr(lse), _ptr(am),
+                                     _ptr(ent), _ptr(workspace), workspace.numel(),
+                                     _stream(stream)), "rlk_logprob_entropy")
+    return lp, lse, am, ent

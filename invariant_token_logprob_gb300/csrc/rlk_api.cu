@@ -300,6 +300,46 @@ rlk_status rlk_logprob(const void* hidden_bf16, const void* weight_bf16,
                                            out_argmax_i32, s));
 }
 
+size_t rlk_logprob_entropy_workspace_size(int64_t T, int64_t H, int64_t V) {
+    if (T <= 0 || V <= 0 || H <= 0) return 0;
+    size_t bytes = partial_bytes(T, V) + (size_t(T) * size_t(num_vocab_tiles(V)) * 4 + 15) / 16 * 16;
+    if (T < rlk::kMinTmaRows) bytes += size_t(rlk::kMinTmaRows) * size_t(H) * 2;
+    return bytes;
+}
+
+rlk_status rlk_logprob_entropy(const void* hidden_bf16, const void* weight_bf16,
+                               const int32_t* targets_i32, int64_t T, int64_t H, int64_t V,
+                               float inv_temp, float* out_logp_f32, float* out_lse_f32,
+                               int32_t* out_argmax_i32, float* out_entropy_f32, void* workspace,
+                               size_t workspace_bytes, rlk_stream_t stream) {
+    rlk_status st = check_shape(T, H, V, inv_temp);
+    if (st != RLK_OK) return st;
+    if (T == 0) return RLK_OK;
+    if ((st = check_operands(hidden_bf16, weight_bf16, targets_i32, H)) != RLK_OK) return st;
+    if ((st = check_outputs(out_logp_f32, out_lse_f32, out_argmax_i32)) != RLK_OK) return st;
+    if (!out_entropy_f32) return RLK_ERR_INVALID_ARG;
+    if (!aligned4(out_entropy_f32)) return RLK_ERR_ALIGNMENT;
+    if (!workspace) return RLK_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return RLK_ERR_ALIGNMENT;
+    if (workspace_bytes < rlk_logprob_entropy_workspace_size(T, H, V)) return RLK_ERR_WORKSPACE;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(workspace);
+    float* ent_u = reinterpret_cast<float*>(base + partial_bytes(T, V));
+    const size_t u_bytes = (size_t(T) * size_t(num_vocab_tiles(V)) * 4 + 15) / 16 * 16;
+    void* pad = T < rlk::kMinTmaRows ? base + partial_bytes(T, V) + u_bytes : nullptr;
+    CUtensorMap th, tw;
+    if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, pad, s, &th, &tw)) != RLK_OK)
+        return st;
+    cudaError_t e = rlk::launch_lmhead_entropy(&th, &tw, targets_i32, workspace, ent_u, T, V, H,
+                                               inv_temp, sms, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(rlk::launch_lse_merge_entropy(workspace, ent_u, targets_i32, T, V,
+                                                   out_logp_f32, out_lse_f32, out_argmax_i32,
+                                                   out_entropy_f32, s));
+}
+
 size_t rlk_logprob_backward_workspace_size(int64_t T, int64_t H, int64_t V) {
     if (T <= 0 || V <= 0 || H <= 0) return 0;
     size_t bytes = (size_t(T) * size_t(V) * 2 + 15) / 16 * 16;

@@ -46,6 +46,19 @@ void release_backward_handles();
 // bounded wait ran out).  Synchronous on the current device.
 cudaError_t lmhead_take_error(unsigned int* out);
 
+// Forward records plus the per-tile entropy statistic ent_u [T][NVT]
+// (sum exp(z - m)(z - m) about the tile's max m).
+cudaError_t launch_lmhead_entropy(const CUtensorMap* th, const CUtensorMap* tw,
+                                  const int32_t* targets, void* partials, float* ent_u, int64_t T,
+                                  int64_t V, int64_t H, float inv_temp, int num_sms,
+                                  cudaStream_t stream);
+
+// Merge with entropy = log S - U / S per row.
+cudaError_t launch_lse_merge_entropy(const void* partials, const float* ent_u,
+                                     const int32_t* targets, int64_t T, int64_t V,
+                                     float* out_logp, float* out_lse, int32_t* out_argmax,
+                                     float* out_entropy, cudaStream_t stream);
+
 // Fixed-tree merge of the partials into logp / lse / argmax.
 cudaError_t launch_lse_merge(const void* partials, const int32_t* targets, int64_t T, int64_t V,
                              float* out_logp, float* out_lse, int32_t* out_argmax,

@@ -64,7 +64,8 @@ __device__ unsigned int g_lmhead_error;
 
 struct Args {
     const int32_t* targets;
-    float4* partials;      // mode 0: [T][num_n] records
+    float4* partials;      // modes 0, 2: [T][num_n] records
+    float* ent_u;          // mode 2: [T][num_n] sum exp(z - m) (z - m) per tile
     const float* lse;      // mode 1: forward LSE per row
     const float* grad;     // mode 1: upstream gradient of logp per row
     uint16_t* dz;          // mode 1: [T][V] bf16 gradient of logp w.r.t. the logits
@@ -126,6 +127,7 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
 // mode sees are the same fp32 values in both.
 constexpr int kModePartials = 0;   // forward: vocabulary-tile partial records
 constexpr int kModeGradLogits = 1; // backward: dz = g (onehot - exp(z - lse)) as bf16
+constexpr int kModeEntropy = 2;    // forward records plus the per-tile entropy statistic
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -275,12 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
 
-            if constexpr (kMode == kModePartials) {
+            if constexpr (kMode == kModePartials || kMode == kModeEntropy) {
                 const int col0 = n * kBN;
                 const int ncols = min(kBN, p.V - col0);
                 const int nchunks = (ncols + 31) >> 5;
                 float run_m = -INFINITY, run_s = 0.0f, zt = 0.0f;
                 int32_t run_a = INT_MAX;
+                float run_u = 0.0f;  // mode 2 only
                 const uint32_t t_addr = lane_base + acc * uint32_t(kBN);
                 for (int c = 0; c < nchunks; ++c) {
                     uint32_t r[32];
@@ -304,9 +307,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ca = j;
                         }
                     const float cml = cm * kLog2e;
-                    float cs = 0.0f;
+                    float cs = 0.0f, cu = 0.0f;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) cs += exp2f(fmaf(z[j], kLog2e, -cml));
+                    for (int j = 0; j < 32; ++j) {
+                        const float e = exp2f(fmaf(z[j], kLog2e, -cml));
+                        cs += e;
+                        if constexpr (kMode == kModeEntropy)
+                            cu = (j < nvalid) ? fmaf(e, z[j] - cm, cu) : cu;
+                    }
                     const int cbase = col0 + c * 32;
                     const int rel = tgt - cbase;
                     if (unsigned(rel) < 32u) {
@@ -314,15 +322,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 32; ++j)
                             if (j == rel) zt = z[j];
                     }
+                    if constexpr (kMode == kModeEntropy)
+                        run_u = lse_combine_u(run_m, run_s, run_a, run_u, cm, cs, cbase + ca, cu);
                     lse_combine(run_m, run_s, run_a, cm, cs, cbase + ca);
                 }
                 // Accumulator buffer fully read: hand it back to the MMA warp.
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty_bar(acc));
-                if (row < p.T)
+                if (row < p.T) {
                     p.partials[row * p.num_n + n] =
                         make_float4(run_m, run_s, __int_as_float(run_a), zt);
+                    if constexpr (kMode == kModeEntropy) p.ent_u[row * p.num_n + n] = run_u;
+                }
             } else {
                 const int col0 = n * kBN;
                 const int ncols = min(kBN, p.V - col0);
@@ -387,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-int g_configured[2][64];  // per mode and device: dynamic shared memory attribute set
+int g_configured[3][64];  // per mode and device: dynamic shared memory attribute set
 
 template <int kMode>
 cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, int64_t H,
@@ -423,6 +435,20 @@ cudaError_t launch_lmhead_partials(const CUtensorMap* th, const CUtensorMap* tw,
     a.V = int(V);
     a.inv_temp = inv_temp;
     return launch_mode<kModePartials>(th, tw, a, H, num_sms, stream);
+}
+
+cudaError_t launch_lmhead_entropy(const CUtensorMap* th, const CUtensorMap* tw,
+                                  const int32_t* targets, void* partials, float* ent_u, int64_t T,
+                                  int64_t V, int64_t H, float inv_temp, int num_sms,
+                                  cudaStream_t stream) {
+    Args a = {};
+    a.targets = targets;
+    a.partials = static_cast<float4*>(partials);
+    a.ent_u = ent_u;
+    a.T = T;
+    a.V = int(V);
+    a.inv_temp = inv_temp;
+    return launch_mode<kModeEntropy>(th, tw, a, H, num_sms, stream);
 }
 
 cudaError_t launch_lmhead_grad_logits(const CUtensorMap* th, const CUtensorMap* tw,

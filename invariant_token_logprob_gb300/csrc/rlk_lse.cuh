@@ -35,4 +35,22 @@ __device__ __forceinline__ void lse_combine(float& m, float& s, int32_t& a, floa
     a = aw;
 }
 
+// Companion of lse_combine for the entropy statistic u = sum exp(z - m) (z - m)
+// of a block taken about its own max m.  Returns the combined u about the
+// winner's max M (same winner rule as lse_combine, evaluated on the values
+// before that call): U = u_win + e^{m_lose - M} (u_lose + (m_lose - M) s_lose).
+// Commutative bit for bit for the same reason as lse_combine.
+__device__ __forceinline__ float lse_combine_u(float m, float s, int32_t a, float u, float m2,
+                                               float s2, int32_t a2, float u2) {
+    const bool other_wins = (m2 > m) || (m2 == m && a2 < a);
+    const float mw = other_wins ? m2 : m;
+    const float uw = other_wins ? u2 : u;
+    const float ml = other_wins ? m : m2;
+    const float sl = other_wins ? s : s2;
+    const float ul = other_wins ? u : u2;
+    if (ml == -INFINITY) return uw;
+    const float d = ml - mw;
+    return uw + exp2f(d * kLog2e) * fmaf(d, sl, ul);
+}
+
 }  // namespace rlk

@@ -10,7 +10,9 @@
 // The tree depends only on NVT = ceil(V / 256), never on T, and lse_combine is
 // commutative bit for bit, so all lanes finish with identical bits.
 //   lse = M + log(S),  argmax = A,  logp = zt(tile of target) - lse
-// (logp = 0 for a target outside [0, V)).
+// (logp = 0 for a target outside [0, V)).  The entropy variant also folds
+// u = sum exp(z - m)(z - m) per tile and writes entropy = log S - U / S, the
+// softmax entropy -sum p log p over the whole vocabulary.
 #include <limits.h>
 
 #include "rlk_internal.h"
@@ -21,19 +23,25 @@ namespace {
 
 constexpr int kMergeWarps = 8;
 
+// kEntropy: also fold the per-tile entropy statistic u (same tree, same winner
+// rule) and write entropy = log S - U / S.
+template <bool kEntropy>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     lse_merge_kernel(const float4* __restrict__ partials, const int32_t* __restrict__ targets,
                      int64_t T, int V, int nvt, float* __restrict__ out_logp,
-                     float* __restrict__ out_lse, int32_t* __restrict__ out_argmax) {
+                     float* __restrict__ out_lse, int32_t* __restrict__ out_argmax,
+                     const float* __restrict__ ent_u, float* __restrict__ out_entropy) {
     const int lane = threadIdx.x & 31;
     const int64_t row = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
     if (row >= T) return;  // whole warp leaves together
     const float4* pr = partials + row * nvt;
 
-    float m = -INFINITY, s = 0.0f;
+    float m = -INFINITY, s = 0.0f, u = 0.0f;
     int32_t a = INT_MAX;
     for (int j = lane; j < nvt; j += 32) {
         const float4 q = __ldg(pr + j);
+        if constexpr (kEntropy)
+            u = lse_combine_u(m, s, a, u, q.x, q.y, __float_as_int(q.z), __ldg(ent_u + row * nvt + j));
         lse_combine(m, s, a, q.x, q.y, __float_as_int(q.z));
     }
 #pragma unroll
@@ -41,6 +49,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
         const float mo = __shfl_xor_sync(0xffffffffu, m, off);
         const float so = __shfl_xor_sync(0xffffffffu, s, off);
         const int32_t ao = __shfl_xor_sync(0xffffffffu, a, off);
+        if constexpr (kEntropy) {
+            const float uo = __shfl_xor_sync(0xffffffffu, u, off);
+            u = lse_combine_u(m, s, a, u, mo, so, ao, uo);
+        }
         lse_combine(m, s, a, mo, so, ao);
     }
     if (lane == 0) {
@@ -51,6 +63,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
         out_logp[row] = logp;
         out_lse[row] = lse;
         out_argmax[row] = a;
+        if constexpr (kEntropy) out_entropy[row] = logf(s) - u / s;
     }
 }
 
@@ -61,9 +74,21 @@ cudaError_t launch_lse_merge(const void* partials, const int32_t* targets, int64
                              cudaStream_t stream) {
     const int nvt = int((V + kVocabTile - 1) / kVocabTile);
     const int64_t blocks = (T + kMergeWarps - 1) / kMergeWarps;
-    lse_merge_kernel<<<unsigned(blocks), kMergeWarps * 32, 0, stream>>>(
+    lse_merge_kernel<false><<<unsigned(blocks), kMergeWarps * 32, 0, stream>>>(
         static_cast<const float4*>(partials), targets, T, int(V), nvt, out_logp, out_lse,
-        out_argmax);
+        out_argmax, nullptr, nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge_entropy(const void* partials, const float* ent_u,
+                                     const int32_t* targets, int64_t T, int64_t V,
+                                     float* out_logp, float* out_lse, int32_t* out_argmax,
+                                     float* out_entropy, cudaStream_t stream) {
+    const int nvt = int((V + kVocabTile - 1) / kVocabTile);
+    const int64_t blocks = (T + kMergeWarps - 1) / kMergeWarps;
+    lse_merge_kernel<true><<<unsigned(blocks), kMergeWarps * 32, 0, stream>>>(
+        static_cast<const float4*>(partials), targets, T, int(V), nvt, out_logp, out_lse,
+        out_argmax, ent_u, out_entropy);
     return cudaGetLastError();
 }
 

@@ -53,6 +53,8 @@ def _bind(lib):
     lib.oracle_consistency_stats.argtypes = [P, P, P, i64, P]
     lib.oracle_logprob_backward.restype = ctypes.c_int
     lib.oracle_logprob_backward.argtypes = [P, P, P, P, i64, i64, i64, ctypes.c_float, P, P, P]
+    lib.oracle_entropy.restype = ctypes.c_int
+    lib.oracle_entropy.argtypes = [P, P, i64, i64, i64, ctypes.c_float, P, i64, P]
     lib.oracle_logprob_f64.restype = ctypes.c_int
     lib.oracle_logprob_f64.argtypes = [P, P, P, i64, i64, i64, ctypes.c_double, P, P]
     return lib
@@ -222,4 +224,21 @@ def logprob_f64(h, W, targets, inv_temp: float = 1.0, lib=None) -> dict:
                                 _ptr(out["logp"]), _ptr(out["lse"]))
     if rc != 0:
         raise ValueError("oracle_logprob_f64 rejected its arguments")
+    return out
+
+
+def entropy(h, W, inv_temp: float = 1.0, rows=None, lib=None) -> np.ndarray:
+    """Per-token softmax entropy over the whole vocabulary (fp64), one per row."""
+    lib = lib or load()
+    h = _u16(h)
+    W = _u16(W)
+    T, H = h.shape
+    V = W.shape[0]
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = T if r is None else r.shape[0]
+    out = np.zeros(n)
+    rc = lib.oracle_entropy(_ptr(h), _ptr(W), T, H, V, ctypes.c_float(inv_temp), _ptr(r), n,
+                            _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_entropy rejected its arguments")
     return out

@@ -342,10 +342,48 @@ def pin_backward_closed_forms(lib):
     assert np.allclose(a["dW"], 2.0 * c["dW"], rtol=1e-13, atol=1e-15)
 
 
+def pin_entropy(lib):
+    """Entropy: W = 0 gives the uniform maximum ln V; a one-hot-dominant row has
+    the two-level closed form; random rows agree with scipy.stats.entropy of the
+    BLAS-computed softmax; an mpmath brute force on integer logits."""
+    import scipy.stats
+    for V in (1, 9, 151936):
+        h = _bf16_bits(np.ones((2, 8), np.float32))
+        e = oracle.entropy(h, np.zeros((V, 8), np.uint16), 1.0, lib=lib)
+        assert np.allclose(e, float(mpmath.log(V)), atol=1e-12)
+    H, V, k, c, b = 16, 500, 3, 2.0, 3.0
+    h = np.zeros((1, H), np.float32)
+    h[0, k] = c
+    W = np.zeros((V, H), np.float32)
+    W[7, k] = b
+    e = oracle.entropy(_bf16_bits(h), _bf16_bits(W), 1.0, lib=lib)
+    zs = mpmath.mpf(b * c)
+    S = mpmath.exp(zs) + (V - 1)
+    p1, q = mpmath.exp(zs) / S, 1 / S
+    assert abs(e[0] - float(-(p1 * mpmath.log(p1)) - (V - 1) * q * mpmath.log(q))) < 1e-12
+    rng = np.random.default_rng(31)
+    hb = _bf16_bits_round(rng.standard_normal((5, 64)).astype(np.float32))
+    Wb = _bf16_bits_round((0.1 * rng.standard_normal((2000, 64))).astype(np.float32))
+    z = (_bits_to_f64(hb) @ _bits_to_f64(Wb).T) * float(np.float32(1 / 0.7))
+    p = scipy.special.softmax(z, axis=1)
+    e = oracle.entropy(hb, Wb, 1 / 0.7, lib=lib)
+    assert np.allclose(e, scipy.stats.entropy(p, axis=1), atol=1e-10)
+    mpmath.mp.dps = 40
+    hi = rng.integers(-3, 4, (2, 6))
+    Wi = rng.integers(-2, 3, (13, 6))
+    e = oracle.entropy(_bf16_bits(hi.astype(np.float32)), _bf16_bits(Wi.astype(np.float32)), 1.0,
+                       lib=lib)
+    for t in range(2):
+        zz = [mpmath.mpf(int(np.dot(hi[t], Wi[v]))) for v in range(13)]
+        lse = mpmath.log(mpmath.fsum(mpmath.exp(x) for x in zz))
+        ent = -mpmath.fsum(mpmath.exp(x - lse) * (x - lse) for x in zz)
+        assert abs(e[t] - float(ent)) < 1e-13
+
+
 PINS = [pin_zero_weights, pin_one_hot_dominant, pin_shift_invariance, pin_temperature,
         pin_brute_force_exact, pin_scipy_logsumexp, pin_ignored_targets,
         pin_block_stats_and_merge, pin_worked_example, pin_stats_closed_forms,
-        pin_backward_finite_differences, pin_backward_closed_forms]
+        pin_backward_finite_differences, pin_backward_closed_forms, pin_entropy]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -375,8 +413,9 @@ def test_pins_catch_planted_mistakes(tmp_path):
     """Each deliberate mistake of oracle.c (ORACLE_MUTANT 1..9: dropped term,
     divided temperature, highest-index ties, LSE without the max, flipped logp
     sign, swapped gap direction, sample variance, backward without inv_temp,
-    unnormalised softmax in the backward) fails at least one pin."""
-    for mutant in range(1, 10):
+    unnormalised softmax in the backward, entropy without the LSE shift) fails at
+    least one pin."""
+    for mutant in range(1, 11):
         path = str(tmp_path / f"liboracle_m{mutant}.so")
         oracle.build(path, mutant=mutant)
         lib = oracle.load(path)
