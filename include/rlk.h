@@ -161,6 +161,40 @@ rlk_status rlk_lse_merge(const rlk_partial *partials, const int32_t *targets_i32
                          int32_t *out_argmax_i32, rlk_stream_t stream);
 
 /*
+ * Vocabulary-sharded (tensor-parallel) form of the two phases.  The RL-Kernel
+ * blog (§七 "LogP") has each vocabulary shard compute local statistics that are
+ * then merged in a fixed vocabulary-tile order; §六 uses a fixed balanced tree
+ * for every TP degree.  Here a shard is a run of whole 256-column tiles of the
+ * one global tile grid, and the merge folds global tiles in exactly the
+ * unsharded order, so the result bits do not depend on the number of shards.
+ *
+ * rlk_logprob_partials_shard: phase 1 on W rows [shard_begin, shard_begin +
+ * shard_rows) given as weight_shard_bf16 ([shard_rows][H], 16-byte aligned).
+ *   shard_begin % rlk_vocab_tile() == 0; shard_rows % rlk_vocab_tile() == 0
+ *   unless the shard ends at V.  targets are global vocabulary indices.
+ *   partials: [T][ceil(shard_rows / rlk_vocab_tile())] records, `a` global.
+ *   Other arguments as rlk_logprob_partials (no small-T staging copy).
+ * rlk_lse_merge_sharded: phase 2 over the shards' partials gathered as
+ *   [num_shards][T][tiles_per_shard] (what an all-gather of the per-shard
+ *   blocks gives); shard r holds global tiles [r * tiles_per_shard, ...), all
+ *   shards but the last hold exactly tiles_per_shard tiles (the last block's
+ *   unused slots are never read).  Requires num_shards * tiles_per_shard >= NVT
+ *   > (num_shards - 1) * tiles_per_shard.  Output bits equal rlk_lse_merge's on
+ *   the unsharded partials.
+ * The exchange between devices (e.g. an NCCL all-gather of T * tiles_per_shard
+ * * 16 bytes per shard) is the caller's.
+ */
+rlk_status rlk_logprob_partials_shard(const void *hidden_bf16, const void *weight_shard_bf16,
+                                      const int32_t *targets_i32, int64_t T, int64_t H, int64_t V,
+                                      int64_t shard_begin, int64_t shard_rows, float inv_temp,
+                                      rlk_partial *partials, size_t partials_bytes,
+                                      rlk_stream_t stream);
+rlk_status rlk_lse_merge_sharded(const rlk_partial *partials, int64_t num_shards,
+                                 int64_t tiles_per_shard, const int32_t *targets_i32, int64_t T,
+                                 int64_t V, float *out_logp_f32, float *out_lse_f32,
+                                 int32_t *out_argmax_i32, rlk_stream_t stream);
+
+/*
  * rlk_logprob plus the per-token entropy of the softmax over the whole
  * vocabulary, entropy[t] = -sum_v p[t][v] log p[t][v] (the actor-entropy signal
  * reported next to rewards in "Finish RL Training Faster: Bitwise-Consistent,

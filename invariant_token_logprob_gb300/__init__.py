@@ -19,7 +19,8 @@ from typing import Optional
 __all__ = ["RlkError", "lib", "logprob", "logprob_ws", "logprob_partials", "lse_merge",
            "consistency_stats", "workspace_size", "check_device_error", "vocab_tile", "row_tile",
            "logprob_backward", "backward_workspace_size", "selected_token_logprob",
-           "logprob_entropy", "entropy_workspace_size",
+           "logprob_entropy", "entropy_workspace_size", "logprob_partials_shard",
+           "lse_merge_sharded",
            "header_functions", "STAT_NAMES", "LIB_PATH", "HEADER_PATH"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -79,6 +80,10 @@ def lib() -> ctypes.CDLL:
         L.rlk_check_device_error.argtypes = [P]
         L.rlk_shutdown.restype = st
         L.rlk_shutdown.argtypes = []
+        L.rlk_logprob_partials_shard.restype = st
+        L.rlk_logprob_partials_shard.argtypes = [P, P, P, i64, i64, i64, i64, i64, f32, P, sz, P]
+        L.rlk_lse_merge_sharded.restype = st
+        L.rlk_lse_merge_sharded.argtypes = [P, i64, i64, P, i64, i64, P, P, P, P]
         L.rlk_logprob_entropy_workspace_size.restype = sz
         L.rlk_logprob_entropy_workspace_size.argtypes = [i64, i64, i64]
         L.rlk_logprob_entropy.restype = st
@@ -331,3 +336,39 @@ def logprob_entropy(h, W, targets, inv_temp: float = 1.0, workspace=None, stream
                                      _ptr(ent), _ptr(workspace), workspace.numel(),
                                      _stream(stream)), "rlk_logprob_entropy")
     return lp, lse, am, ent
+
+
+def logprob_partials_shard(h, W_shard, targets, V: int, shard_begin: int, inv_temp: float = 1.0,
+                           out=None, stream=None):
+    """rlk_logprob_partials_shard: partials [T, ceil(rows/vocab_tile), 4] of one
+    vocabulary shard W_shard = W[shard_begin : shard_begin + rows]."""
+    import torch
+    _need(h, torch.bfloat16, "h", 2)
+    _need(W_shard, torch.bfloat16, "W_shard", 2)
+    _need(targets, torch.int32, "targets", 1)
+    T, H = h.shape
+    rows = W_shard.shape[0]
+    nvt_s = (rows + vocab_tile() - 1) // vocab_tile()
+    if out is None:
+        out = torch.empty((T, nvt_s, 4), dtype=torch.float32, device=h.device)
+    _need(out, torch.float32, "out")
+    _check(lib().rlk_logprob_partials_shard(_ptr(h), _ptr(W_shard), _ptr(targets), T, H, int(V),
+                                            int(shard_begin), rows, ctypes.c_float(inv_temp),
+                                            _ptr(out), out.numel() * 4, _stream(stream)),
+           "rlk_logprob_partials_shard")
+    return out
+
+
+def lse_merge_sharded(partials, targets, V: int, out=None, stream=None):
+    """rlk_lse_merge_sharded over gathered partials [R, T, tiles_per_shard, 4]."""
+    import torch
+    _need(partials, torch.float32, "partials", 4)
+    _need(targets, torch.int32, "targets", 1)
+    R, T, nvt_s, four = partials.shape
+    if four != 4 or targets.shape[0] != T:
+        raise ValueError("partials must be [R, T, tiles_per_shard, 4] and targets [T]")
+    lp, lse, am = _outputs(T, partials.device, out)
+    _check(lib().rlk_lse_merge_sharded(_ptr(partials), R, nvt_s, _ptr(targets), T, int(V),
+                                       _ptr(lp), _ptr(lse), _ptr(am), _stream(stream)),
+           "rlk_lse_merge_sharded")
+    return lp, lse, am

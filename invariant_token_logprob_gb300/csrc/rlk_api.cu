@@ -300,6 +300,54 @@ rlk_status rlk_logprob(const void* hidden_bf16, const void* weight_bf16,
                                            out_argmax_i32, s));
 }
 
+rlk_status rlk_logprob_partials_shard(const void* hidden_bf16, const void* weight_shard_bf16,
+                                      const int32_t* targets_i32, int64_t T, int64_t H, int64_t V,
+                                      int64_t shard_begin, int64_t shard_rows, float inv_temp,
+                                      rlk_partial* partials, size_t partials_bytes,
+                                      rlk_stream_t stream) {
+    rlk_status st = check_shape(T, H, V, inv_temp);
+    if (st != RLK_OK) return st;
+    if (shard_begin < 0 || shard_rows < 1 || shard_begin + shard_rows > V) return RLK_ERR_INVALID_ARG;
+    // a shard holds whole tiles of the global vocabulary-tile grid
+    if (shard_begin % kVocabTile != 0) return RLK_ERR_INVALID_ARG;
+    if (shard_rows % kVocabTile != 0 && shard_begin + shard_rows != V) return RLK_ERR_INVALID_ARG;
+    if (T == 0) return RLK_OK;
+    if ((st = check_operands(hidden_bf16, weight_shard_bf16, targets_i32, H)) != RLK_OK) return st;
+    if (!partials) return RLK_ERR_INVALID_ARG;
+    if (!aligned16(partials)) return RLK_ERR_ALIGNMENT;
+    if (partials_bytes < partial_bytes(T, shard_rows)) return RLK_ERR_WORKSPACE;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUtensorMap th, tw;
+    if ((st = prepare_maps(hidden_bf16, weight_shard_bf16, T, H, shard_rows, nullptr, s, &th,
+                           &tw)) != RLK_OK)
+        return st;
+    return from_cuda(rlk::launch_lmhead_partials(&th, &tw, targets_i32, partials, T, shard_rows, H,
+                                                 inv_temp, sms, s, shard_begin));
+}
+
+rlk_status rlk_lse_merge_sharded(const rlk_partial* partials, int64_t num_shards,
+                                 int64_t tiles_per_shard, const int32_t* targets_i32, int64_t T,
+                                 int64_t V, float* out_logp_f32, float* out_lse_f32,
+                                 int32_t* out_argmax_i32, rlk_stream_t stream) {
+    if (T < 0 || V < 1 || V > INT32_MAX || T > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    const int64_t nvt = num_vocab_tiles(V);
+    if (num_shards < 1 || tiles_per_shard < 1 || num_shards * tiles_per_shard < nvt ||
+        (num_shards - 1) * tiles_per_shard >= nvt)
+        return RLK_ERR_INVALID_ARG;
+    if (T == 0) return RLK_OK;
+    if (!partials || !targets_i32) return RLK_ERR_INVALID_ARG;
+    rlk_status st = check_outputs(out_logp_f32, out_lse_f32, out_argmax_i32);
+    if (st != RLK_OK) return st;
+    if (!aligned16(partials) || !aligned4(targets_i32)) return RLK_ERR_ALIGNMENT;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    return from_cuda(rlk::launch_lse_merge_sharded(partials, int(tiles_per_shard), targets_i32, T,
+                                                   V, out_logp_f32, out_lse_f32, out_argmax_i32,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t rlk_logprob_entropy_workspace_size(int64_t T, int64_t H, int64_t V) {
     if (T <= 0 || V <= 0 || H <= 0) return 0;
     size_t bytes = partial_bytes(T, V) + (size_t(T) * size_t(num_vocab_tiles(V)) * 4 + 15) / 16 * 16;

@@ -23,9 +23,21 @@ cudaError_t launch_pad_rows(const void* h, int64_t T, int64_t H, void* dst, cuda
 // Fused LM-head GEMM + vocabulary-tile epilogue.  Writes partials[T][NVT]
 // (16-byte records {m, s, a, zt}).  th / tw are 2-D tensor maps of h [T,H] and
 // W [V,H] with boxes {kKBlock, kRowTile} / {kKBlock, kVocabTile}, 128-B swizzle.
+// col_offset: global vocabulary index of tw's row 0 when tw maps a shard of W
+// (a multiple of kVocabTile); record indices `a` and target matching use global
+// columns, V is the number of rows tw maps.
 cudaError_t launch_lmhead_partials(const CUtensorMap* th, const CUtensorMap* tw,
                                    const int32_t* targets, void* partials, int64_t T, int64_t V,
-                                   int64_t H, float inv_temp, int num_sms, cudaStream_t stream);
+                                   int64_t H, float inv_temp, int num_sms, cudaStream_t stream,
+                                   int64_t col_offset = 0);
+
+// Merge of partials gathered from R vocabulary shards, laid out [R][T][nvt_shard]
+// (shard r holds global tiles [r*nvt_shard, (r+1)*nvt_shard)); the fold order over
+// global tiles is the unsharded one, so the bits equal the unsharded merge's.
+cudaError_t launch_lse_merge_sharded(const void* partials, int nvt_shard,
+                                     const int32_t* targets, int64_t T, int64_t V,
+                                     float* out_logp, float* out_lse, int32_t* out_argmax,
+                                     cudaStream_t stream);
 
 // Same main loop with the backward epilogue: recomputes the logits and writes
 // dz[t][v] = grad[t] * ([v == target[t]] - exp(z[t][v] - lse[t])) as bf16

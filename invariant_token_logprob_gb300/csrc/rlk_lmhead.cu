@@ -70,7 +70,8 @@ struct Args {
     const float* grad;     // mode 1: upstream gradient of logp per row
     uint16_t* dz;          // mode 1: [T][V] bf16 gradient of logp w.r.t. the logits
     int64_t T;
-    int V;
+    int V;          // columns of the W this launch sees (a shard's rows when sharded)
+    int col_offset; // global vocabulary index of that W's row 0 (0 unless sharded)
     int num_m;   // row tiles
     int num_n;   // vocabulary tiles (NVT)
     int num_kb;  // k-blocks
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (kMode == kModeEntropy)
                             cu = (j < nvalid) ? fmaf(e, z[j] - cm, cu) : cu;
                     }
-                    const int cbase = col0 + c * 32;
+                    const int cbase = p.col_offset + col0 + c * 32;  // global column of j = 0
                     const int rel = tgt - cbase;
                     if (unsigned(rel) < 32u) {
 #pragma unroll
@@ -427,12 +428,14 @@ cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, in
 
 cudaError_t launch_lmhead_partials(const CUtensorMap* th, const CUtensorMap* tw,
                                    const int32_t* targets, void* partials, int64_t T, int64_t V,
-                                   int64_t H, float inv_temp, int num_sms, cudaStream_t stream) {
+                                   int64_t H, float inv_temp, int num_sms, cudaStream_t stream,
+                                   int64_t col_offset) {
     Args a = {};
     a.targets = targets;
     a.partials = static_cast<float4*>(partials);
     a.T = T;
     a.V = int(V);
+    a.col_offset = int(col_offset);
     a.inv_temp = inv_temp;
     return launch_mode<kModePartials>(th, tw, a, H, num_sms, stream);
 }

@@ -23,23 +23,37 @@ namespace {
 
 constexpr int kMergeWarps = 8;
 
+// Record of global tile j for `row`: [T][nvt] unsharded, or [R][T][nvt_shard]
+// when the partials were gathered from vocabulary shards.
+template <bool kSharded>
+__device__ __forceinline__ const float4* record(const float4* partials, int64_t row, int64_t T,
+                                                int nvt, int nvt_shard, int j) {
+    if constexpr (kSharded) {
+        const int r = j / nvt_shard;
+        return partials + (int64_t(r) * T + row) * nvt_shard + (j - r * nvt_shard);
+    } else {
+        return partials + row * nvt + j;
+    }
+}
+
 // kEntropy: also fold the per-tile entropy statistic u (same tree, same winner
-// rule) and write entropy = log S - U / S.
-template <bool kEntropy>
+// rule) and write entropy = log S - U / S.  kSharded: records gathered from
+// vocabulary shards (same global tiles, same fold order, same bits).
+template <bool kEntropy, bool kSharded = false>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     lse_merge_kernel(const float4* __restrict__ partials, const int32_t* __restrict__ targets,
                      int64_t T, int V, int nvt, float* __restrict__ out_logp,
                      float* __restrict__ out_lse, int32_t* __restrict__ out_argmax,
-                     const float* __restrict__ ent_u, float* __restrict__ out_entropy) {
+                     const float* __restrict__ ent_u, float* __restrict__ out_entropy,
+                     int nvt_shard = 0) {
     const int lane = threadIdx.x & 31;
     const int64_t row = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
     if (row >= T) return;  // whole warp leaves together
-    const float4* pr = partials + row * nvt;
 
     float m = -INFINITY, s = 0.0f, u = 0.0f;
     int32_t a = INT_MAX;
     for (int j = lane; j < nvt; j += 32) {
-        const float4 q = __ldg(pr + j);
+        const float4 q = __ldg(record<kSharded>(partials, row, T, nvt, nvt_shard, j));
         if constexpr (kEntropy)
             u = lse_combine_u(m, s, a, u, q.x, q.y, __float_as_int(q.z), __ldg(ent_u + row * nvt + j));
         lse_combine(m, s, a, q.x, q.y, __float_as_int(q.z));
@@ -59,7 +73,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
         const float lse = m + logf(s);
         const int32_t tgt = __ldg(targets + row);
         float logp = 0.0f;
-        if (tgt >= 0 && tgt < V) logp = __ldg(pr + tgt / kVocabTile).w - lse;
+        if (tgt >= 0 && tgt < V)
+            logp = __ldg(record<kSharded>(partials, row, T, nvt, nvt_shard, tgt / kVocabTile)).w -
+                   lse;
         out_logp[row] = logp;
         out_lse[row] = lse;
         out_argmax[row] = a;
@@ -77,6 +93,18 @@ cudaError_t launch_lse_merge(const void* partials, const int32_t* targets, int64
     lse_merge_kernel<false><<<unsigned(blocks), kMergeWarps * 32, 0, stream>>>(
         static_cast<const float4*>(partials), targets, T, int(V), nvt, out_logp, out_lse,
         out_argmax, nullptr, nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge_sharded(const void* partials, int nvt_shard,
+                                     const int32_t* targets, int64_t T, int64_t V,
+                                     float* out_logp, float* out_lse, int32_t* out_argmax,
+                                     cudaStream_t stream) {
+    const int nvt = int((V + kVocabTile - 1) / kVocabTile);
+    const int64_t blocks = (T + kMergeWarps - 1) / kMergeWarps;
+    lse_merge_kernel<false, true><<<unsigned(blocks), kMergeWarps * 32, 0, stream>>>(
+        static_cast<const float4*>(partials), targets, T, int(V), nvt, out_logp, out_lse,
+        out_argmax, nullptr, nullptr, nvt_shard);
     return cudaGetLastError();
 }
 
