@@ -305,6 +305,20 @@ rlk_status rlk_logprob_noalloc(const void *hidden_bf16, const void *weight_bf16,
  */
 rlk_status rlk_check_device_error(rlk_stream_t stream);
 
+/*
+ * Self-test of the failure detection above, for test suites: launches the
+ * forward kernel on a 1 x 64 x 256 problem with its copy engine told to issue
+ * nothing, so the first wait for data can only end by running out its time
+ * limit (about 2 s).  The kernel then records the timeout, releases its tensor
+ * memory and returns; no copy is left in flight and the context stays usable.
+ * A following rlk_check_device_error(stream) returns RLK_ERR_TIMEOUT.
+ *   hidden_bf16 [1][64], weight_bf16 [256][64] (16-byte aligned), targets_i32 [1],
+ *   partials (16-byte aligned, >= 16 bytes; left unwritten): device buffers.
+ */
+rlk_status rlk_selftest_wait_timeout(const void *hidden_bf16, const void *weight_bf16,
+                                     const int32_t *targets_i32, rlk_partial *partials,
+                                     rlk_stream_t stream);
+
 /* Release the library's cached workspaces on every device it used (waits for
  * them to be idle).  Safe to call more than once. */
 rlk_status rlk_shutdown(void);

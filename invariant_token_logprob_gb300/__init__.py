@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.rlk_lse_merge.argtypes = [P, P, i64, i64, P, P, P, P]
         L.rlk_consistency_stats.restype = st
         L.rlk_consistency_stats.argtypes = [P, P, P, i64, P, P]
+        L.rlk_selftest_wait_timeout.restype = st
+        L.rlk_selftest_wait_timeout.argtypes = [P, P, P, P, P]
         L.rlk_check_device_error.restype = st
         L.rlk_check_device_error.argtypes = [P]
         L.rlk_shutdown.restype = st

@@ -445,6 +445,24 @@ rlk_status rlk_consistency_stats(const float* logp_a, const float* logp_b, const
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
+rlk_status rlk_selftest_wait_timeout(const void* hidden_bf16, const void* weight_bf16,
+                                     const int32_t* targets_i32, rlk_partial* partials,
+                                     rlk_stream_t stream) {
+    constexpr int64_t T = 1, H = 64, V = 256;
+    rlk_status st = check_operands(hidden_bf16, weight_bf16, targets_i32, H);
+    if (st != RLK_OK) return st;
+    if (!partials) return RLK_ERR_INVALID_ARG;
+    if (!aligned16(partials)) return RLK_ERR_ALIGNMENT;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUtensorMap th, tw;
+    if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, nullptr, s, &th, &tw)) != RLK_OK)
+        return st;
+    return from_cuda(rlk::launch_lmhead_stall_selftest(&th, &tw, targets_i32, partials, T, V, H,
+                                                       sms, s));
+}
+
 rlk_status rlk_check_device_error(rlk_stream_t stream) {
     int dev, sms;
     rlk_status st = current_device(&dev, &sms);

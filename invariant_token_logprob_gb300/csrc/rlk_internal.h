@@ -54,6 +54,13 @@ cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, int
                                float* grad_W, bool accumulate_W, cudaStream_t stream);
 void release_backward_handles();
 
+// Bounded-wait self-test: the forward kernel with its producer issuing no
+// copies, so the MMA warp's wait runs out (kernel error word bit 0) after its
+// time limit and every role returns.
+cudaError_t launch_lmhead_stall_selftest(const CUtensorMap* th, const CUtensorMap* tw,
+                                         const int32_t* targets, void* partials, int64_t T,
+                                         int64_t V, int64_t H, int num_sms, cudaStream_t stream);
+
 // Reads and clears the per-device error word of the LM-head kernel (bit 0: a
 // bounded wait ran out).  Synchronous on the current device.
 cudaError_t lmhead_take_error(unsigned int* out);

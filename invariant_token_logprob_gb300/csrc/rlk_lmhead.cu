@@ -78,6 +78,7 @@ struct Args {
     int band;    // row tiles per raster band (schedule only; never affects values)
     int num_tiles;
     float inv_temp;
+    int stall_selftest;  // 1: the producer issues no copies (bounded-wait self-test)
 };
 
 // Raster: bands of `band` row tiles; inside a band, vocabulary tile outer and
@@ -191,7 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            // Self-test: no copy is ever issued, so the MMA warp's first wait can
+            // only end by running out; everything else then sees the abort flag.
+            const int ntiles = p.stall_selftest ? 0 : p.num_tiles;
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
                 int m, n;
                 tile_coords(p, tile, m, n);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -452,6 +456,19 @@ cudaError_t launch_lmhead_entropy(const CUtensorMap* th, const CUtensorMap* tw,
     a.V = int(V);
     a.inv_temp = inv_temp;
     return launch_mode<kModeEntropy>(th, tw, a, H, num_sms, stream);
+}
+
+cudaError_t launch_lmhead_stall_selftest(const CUtensorMap* th, const CUtensorMap* tw,
+                                         const int32_t* targets, void* partials, int64_t T,
+                                         int64_t V, int64_t H, int num_sms, cudaStream_t stream) {
+    Args a = {};
+    a.targets = targets;
+    a.partials = static_cast<float4*>(partials);
+    a.T = T;
+    a.V = int(V);
+    a.inv_temp = 1.0f;
+    a.stall_selftest = 1;
+    return launch_mode<kModePartials>(th, tw, a, H, num_sms, stream);
 }
 
 cudaError_t launch_lmhead_grad_logits(const CUtensorMap* th, const CUtensorMap* tw,
