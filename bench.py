@@ -280,7 +280,8 @@ def time_decode(rlk, torch, W, Ts, reps, rounds, stream):
     return {T: statistics.median(v) for T, v in times.items()}
 
 
-def decode_points(rlk, torch, W, stream, pk, Ts=(1, 2, 4, 8, 16), reps=50, rounds=3):
+def decode_points(rlk, torch, W, stream, pk, Ts=(1, 2, 4, 8, 16, 32, 64, 128, 256), reps=50,
+                  rounds=3):
     wbytes = V_CFG * H_CFG * 2
     res = {}
     for T, s in time_decode(rlk, torch, W, Ts, reps, rounds, stream).items():

@@ -185,6 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above touched only shared memory, TMEM and the kernel
+    // parameters; the launch may overlap the previous kernel in the stream up to
+    // here.  No global memory is read or written before this wait.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -424,7 +429,18 @@ cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, in
     a.band = a.num_m < 32 ? a.num_m : 32;
     a.num_tiles = a.num_m * a.num_n;
     const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
-    lmhead_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(*th, *tw, a);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, lmhead_kernel<kMode>, *th, *tw, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

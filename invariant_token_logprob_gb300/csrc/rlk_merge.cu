@@ -17,6 +17,7 @@
 
 #include "rlk_internal.h"
 #include "rlk_lse.cuh"
+#include "rlk_sm103.cuh"
 
 namespace rlk {
 namespace {
@@ -46,17 +47,39 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
                      float* __restrict__ out_lse, int32_t* __restrict__ out_argmax,
                      const float* __restrict__ ent_u, float* __restrict__ out_entropy,
                      int nvt_shard = 0) {
+    // Launched with programmatic overlap: wait for the producer of the partials
+    // before reading anything, then let the next kernel start its launch.
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t row = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
     if (row >= T) return;  // whole warp leaves together
 
     float m = -INFINITY, s = 0.0f, u = 0.0f;
     int32_t a = INT_MAX;
-    for (int j = lane; j < nvt; j += 32) {
-        const float4 q = __ldg(record<kSharded>(partials, row, T, nvt, nvt_shard, j));
-        if constexpr (kEntropy)
-            u = lse_combine_u(m, s, a, u, q.x, q.y, __float_as_int(q.z), __ldg(ent_u + row * nvt + j));
-        lse_combine(m, s, a, q.x, q.y, __float_as_int(q.z));
+    // Lane l folds tiles l, l+32, l+64, ... in ascending order.  The records are
+    // fetched kBatch at a time before folding them (same order, same bits), so a
+    // row costs a few memory round trips instead of one per tile.
+    constexpr int kBatch = 8;
+    for (int j0 = lane; j0 < nvt; j0 += 32 * kBatch) {
+        float4 q[kBatch];
+        float uq[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int j = j0 + 32 * b;
+            if (j < nvt) {
+                q[b] = __ldg(record<kSharded>(partials, row, T, nvt, nvt_shard, j));
+                if constexpr (kEntropy) uq[b] = __ldg(ent_u + row * nvt + j);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if (j0 + 32 * b < nvt) {
+                if constexpr (kEntropy)
+                    u = lse_combine_u(m, s, a, u, q[b].x, q[b].y, __float_as_int(q[b].z), uq[b]);
+                lse_combine(m, s, a, q[b].x, q[b].y, __float_as_int(q[b].z));
+            }
+        }
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
@@ -83,17 +106,38 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     }
 }
 
+template <bool kEntropy, bool kSharded>
+cudaError_t launch_merge(int64_t T, cudaStream_t stream, const float4* partials,
+                         const int32_t* targets, int V, int nvt, float* out_logp, float* out_lse,
+                         int32_t* out_argmax, const float* ent_u, float* out_entropy,
+                         int nvt_shard) {
+    const int64_t blocks = (T + kMergeWarps - 1) / kMergeWarps;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(unsigned(blocks), 1, 1);
+    cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, lse_merge_kernel<kEntropy, kSharded>, partials,
+                                       targets, T, V, nvt, out_logp, out_lse, out_argmax, ent_u,
+                                       out_entropy, nvt_shard);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_lse_merge(const void* partials, const int32_t* targets, int64_t T, int64_t V,
                              float* out_logp, float* out_lse, int32_t* out_argmax,
                              cudaStream_t stream) {
     const int nvt = int((V + kVocabTile - 1) / kVocabTile);
-    const int64_t blocks = (T + kMergeWarps - 1) / kMergeWarps;
-    lse_merge_kernel<false><<<unsigned(blocks), kMergeWarps * 32, 0, stream>>>(
-        static_cast<const float4*>(partials), targets, T, int(V), nvt, out_logp, out_lse,
-        out_argmax, nullptr, nullptr);
-    return cudaGetLastError();
+    return launch_merge<false, false>(T, stream, static_cast<const float4*>(partials), targets,
+                                      int(V), nvt, out_logp, out_lse, out_argmax, nullptr, nullptr,
+                                      0);
 }
 
 cudaError_t launch_lse_merge_sharded(const void* partials, int nvt_shard,
@@ -101,11 +145,9 @@ cudaError_t launch_lse_merge_sharded(const void* partials, int nvt_shard,
                                      float* out_logp, float* out_lse, int32_t* out_argmax,
                                      cudaStream_t stream) {
     const int nvt = int((V + kVocabTile - 1) / kVocabTile);
-    const int64_t blocks = (T + kMergeWarps - 1) / kMergeWarps;
-    lse_merge_kernel<false, true><<<unsigned(blocks), kMergeWarps * 32, 0, stream>>>(
-        static_cast<const float4*>(partials), targets, T, int(V), nvt, out_logp, out_lse,
-        out_argmax, nullptr, nullptr, nvt_shard);
-    return cudaGetLastError();
+    return launch_merge<false, true>(T, stream, static_cast<const float4*>(partials), targets,
+                                     int(V), nvt, out_logp, out_lse, out_argmax, nullptr, nullptr,
+                                     nvt_shard);
 }
 
 cudaError_t launch_lse_merge_entropy(const void* partials, const float* ent_u,
@@ -113,11 +155,9 @@ cudaError_t launch_lse_merge_entropy(const void* partials, const float* ent_u,
                                      float* out_logp, float* out_lse, int32_t* out_argmax,
                                      float* out_entropy, cudaStream_t stream) {
     const int nvt = int((V + kVocabTile - 1) / kVocabTile);
-    const int64_t blocks = (T + kMergeWarps - 1) / kMergeWarps;
-    lse_merge_kernel<true><<<unsigned(blocks), kMergeWarps * 32, 0, stream>>>(
-        static_cast<const float4*>(partials), targets, T, int(V), nvt, out_logp, out_lse,
-        out_argmax, ent_u, out_entropy);
-    return cudaGetLastError();
+    return launch_merge<true, false>(T, stream, static_cast<const float4*>(partials), targets,
+                                     int(V), nvt, out_logp, out_lse, out_argmax, ent_u, out_entropy,
+                                     0);
 }
 
 }  // namespace rlk

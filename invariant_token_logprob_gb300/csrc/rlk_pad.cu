@@ -9,6 +9,7 @@
 // tiles byte-for-byte the same as before (zeros either way), so no result bit
 // can change; only where the zeros come from does.
 #include "rlk_internal.h"
+#include "rlk_sm103.cuh"
 
 namespace rlk {
 namespace {
@@ -16,6 +17,9 @@ namespace {
 __global__ void __launch_bounds__(256)
     pad_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n_src,
                     int64_t n_dst) {
+    // The LM-head kernel that follows may start its set-up now; it waits for this
+    // grid to finish before it reads the padded rows.
+    grid_launch_dependents();
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_dst;
          i += int64_t(gridDim.x) * blockDim.x)
         dst[i] = i < n_src ? src[i] : make_uint4(0u, 0u, 0u, 0u);

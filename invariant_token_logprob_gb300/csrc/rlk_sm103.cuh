@@ -21,6 +21,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Block until the grids this one depends on have completed and their memory
+// is visible (a no-op when the launch did not allow programmatic overlap).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the next grid in the stream (if launched with programmatic overlap)
+// start its launch now; its own griddepcontrol.wait still orders its reads.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
