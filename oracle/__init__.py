@@ -55,6 +55,11 @@ def _bind(lib):
     lib.oracle_logprob_backward.argtypes = [P, P, P, P, i64, i64, i64, ctypes.c_float, P, P, P]
     lib.oracle_entropy.restype = ctypes.c_int
     lib.oracle_entropy.argtypes = [P, P, i64, i64, i64, ctypes.c_float, P, i64, P]
+    lib.oracle_quantize_fp8_rows.restype = ctypes.c_int
+    lib.oracle_quantize_fp8_rows.argtypes = [P, i64, i64, P, P]
+    lib.oracle_logprob_fp8.restype = ctypes.c_int
+    lib.oracle_logprob_fp8.argtypes = [P, P, P, P, P, i64, i64, i64, ctypes.c_float, P, i64,
+                                       P, P, P, P]
     lib.oracle_logprob_f64.restype = ctypes.c_int
     lib.oracle_logprob_f64.argtypes = [P, P, P, i64, i64, i64, ctypes.c_double, P, P]
     return lib
@@ -241,4 +246,39 @@ def entropy(h, W, inv_temp: float = 1.0, rows=None, lib=None) -> np.ndarray:
                             _ptr(out))
     if rc != 0:
         raise ValueError("oracle_entropy rejected its arguments")
+    return out
+
+
+def quantize_fp8_rows(x, lib=None):
+    """Per-row e4m3 quantisation of a bf16 matrix: (codes uint8 [rows,H], scales f32 [rows])."""
+    lib = lib or load()
+    x = _u16(x)
+    rows, H = x.shape
+    codes = np.zeros((rows, H), dtype=np.uint8)
+    scales = np.zeros(rows, dtype=np.float32)
+    rc = lib.oracle_quantize_fp8_rows(_ptr(x), rows, H, _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError("oracle_quantize_fp8_rows rejected its arguments")
+    return codes, scales
+
+
+def logprob_fp8(qh, sh, qw, sw, targets, inv_temp: float = 1.0, rows=None, lib=None) -> dict:
+    """Selected-token logprob from e4m3 codes and per-row scales (fp64)."""
+    lib = lib or load()
+    qh = np.ascontiguousarray(qh, dtype=np.uint8)
+    qw = np.ascontiguousarray(qw, dtype=np.uint8)
+    sh = np.ascontiguousarray(sh, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    tg = _i32(targets)
+    T, H = qh.shape
+    V = qw.shape[0]
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = T if r is None else r.shape[0]
+    out = {k: np.zeros(n) for k in ("logp", "lse", "top2gap")}
+    out["argmax"] = np.zeros(n, dtype=np.int64)
+    rc = lib.oracle_logprob_fp8(_ptr(qh), _ptr(sh), _ptr(qw), _ptr(sw), _ptr(tg), T, H, V,
+                                ctypes.c_float(inv_temp), _ptr(r), n, _ptr(out["logp"]),
+                                _ptr(out["lse"]), _ptr(out["argmax"]), _ptr(out["top2gap"]))
+    if rc != 0:
+        raise ValueError("oracle_logprob_fp8 rejected its arguments")
     return out

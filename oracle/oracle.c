@@ -527,3 +527,113 @@ int oracle_entropy(const uint16_t *h, const uint16_t *W, int64_t T, int64_t H, i
     }
     return bad ? -1 : 0;
 }
+
+
+/* ------------------------------------------------------------------------
+ * FP8 (W8A8) variant.  The consistency blog runs its dense layers as
+ * block-FP8 W8A8 GEMMs with round-to-nearest-even quantisation and one fixed
+ * accumulation order per output ("Finish RL Training Faster ...", sections on
+ * the dense GEMM and the expert GEMM: RNE quantisation, fixed accumulation
+ * tree).  Reading taken here for the LM head: one fp32 scale per row of h
+ * (per token) and per row of W (per vocabulary entry), s = amax / 448 (s = 1
+ * for an all-zero row), code = RNE-to-e4m3(x / s) with the division in fp32,
+ * saturating at +-448.  z = (sum_k qh[k] qW[k]) * s_h * s_W * inv_temp.
+ */
+
+/* Value of an e4m3 code (1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
+ * no infinities; exponent 15 with mantissa 7 is NaN). */
+static double e4m3_value(uint8_t c)
+{
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);            /* subnormal: m/8 * 2^-6 */
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Round a float to the nearest e4m3 value, ties to an even mantissa,
+ * saturating at +-448: by scanning the 127 non-negative finite codes. */
+static uint8_t e4m3_rne(float x)
+{
+    double ax = fabs((double)x);
+    uint8_t best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 126; ++c) {
+        double d = fabs(e4m3_value((uint8_t)c) - ax);
+        if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) { bd = d; best = (uint8_t)c; }
+    }
+#if ORACLE_MUTANT == 11
+    best = (uint8_t)(ax > e4m3_value(best) && best < 126 ? best + 1 : best); /* mutant: rounds up */
+#endif
+    if (ax > 448.0) best = 126;                      /* saturate to 448 */
+    /* rounding keeps the operand's sign, also when the magnitude rounds to 0 */
+    return (uint8_t)(best | (signbit(x) ? 0x80 : 0));
+}
+
+/* Quantise rows of a bf16 matrix [rows][H]: codes [rows][H], scales [rows]. */
+int oracle_quantize_fp8_rows(const uint16_t *x, int64_t rows, int64_t H, uint8_t *codes,
+                             float *scales)
+{
+    if (!x || !codes || !scales || rows < 0 || H <= 0) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < H; ++k) {
+            float v = (float)bf16_to_double(x[r * H + k]);
+            if (fabsf(v) > amax) amax = fabsf(v);
+        }
+        float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scales[r] = sc;
+        for (int64_t k = 0; k < H; ++k) {
+            float v = (float)bf16_to_double(x[r * H + k]);
+            codes[r * H + k] = e4m3_rne(v / sc);
+        }
+    }
+    return 0;
+}
+
+/* Selected-token logprob from quantised operands, by definition in fp64. */
+int oracle_logprob_fp8(const uint8_t *qh, const float *sh, const uint8_t *qw, const float *sw,
+                       const int32_t *targets, int64_t T, int64_t H, int64_t V, float inv_temp,
+                       const int64_t *rows, int64_t n_rows, double *out_logp, double *out_lse,
+                       int64_t *out_argmax, double *out_top2gap)
+{
+    if (!qh || !sh || !qw || !sw || !targets || T < 0 || H <= 0 || V <= 0 || n_rows < 0)
+        return -1;
+    if (!rows && n_rows != T) return -1;
+    double lut[256];
+    for (int c = 0; c < 256; ++c) lut[c] = e4m3_value((uint8_t)c);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *z = (double *)malloc((size_t)V * sizeof(double));
+        if (!z) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_rows; ++i) {
+            if (!z) continue;
+            int64_t t = rows ? rows[i] : i;
+            if (t < 0 || t >= T) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            for (int64_t v = 0; v < V; ++v) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < H; ++k)
+                    acc += lut[qh[t * H + k]] * lut[qw[v * H + k]];
+                z[v] = acc * (double)sh[t] * (double)sw[v] * (double)inv_temp;
+            }
+            row_result r = logprob_row(z, V, targets[t]);
+            if (out_logp) out_logp[i] = r.logp;
+            if (out_lse) out_lse[i] = r.lse;
+            if (out_argmax) out_argmax[i] = r.argmax;
+            if (out_top2gap) out_top2gap[i] = r.top2gap;
+        }
+        free(z);
+    }
+    return bad ? -1 : 0;
+}

@@ -380,10 +380,82 @@ def pin_entropy(lib):
         assert abs(e[t] - float(ent)) < 1e-13
 
 
+def _e4m3_table():
+    """All 256 e4m3 values decoded by PyTorch's float8_e4m3fn (a library routine)."""
+    import torch
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
+def pin_fp8_quantiser(lib):
+    """Per-row e4m3 quantisation: scale = amax/448 in fp32 (1 for a zero row);
+    each code is the nearest e4m3 value to x/s (fp32 division), ties to the even
+    code, by brute force over all codes; agrees with torch's RNE cast."""
+    import torch
+    tab = _e4m3_table()
+    finite = np.isfinite(tab)
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((6, 96)).astype(np.float32) * np.array([1, 10, 1e-3, 300, 1, 0])[:, None]
+    x[4, :8] = [0.5, -0.5, 1.0, 3.0, -448.0, 2.0, 0.0, 7.0]  # exact values and a tie pattern
+    x[4, 8:12] = [-0.0, -1e-30, 1e-30, -3e-5]                # signed zeros and underflow to 0
+    xb = _bf16_bits_round(x)
+    codes, scales = oracle.quantize_fp8_rows(xb, lib=lib)
+    xf = _bits_to_f64(xb).astype(np.float32)
+    for r in range(6):
+        amax = np.float32(np.max(np.abs(xf[r])))
+        exp_s = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+        assert scales[r] == exp_s
+        y = (xf[r] / scales[r]).astype(np.float32).astype(np.float64)
+        for k in range(96):
+            d = np.where(finite, np.abs(tab - y[k]), np.inf)
+            best = np.flatnonzero(d == d.min())
+            want = [c for c in best if c & 1 == 0] or list(best)
+            got = codes[r, k] & 0x7F if y[k] <= 0 and tab[codes[r, k]] <= 0 else codes[r, k]
+            want = [c & 0x7F for c in want] if y[k] <= 0 else want
+            assert got in want or (y[k] == 0 and tab[codes[r, k]] == 0), (r, k, y[k])
+        ref = torch.from_numpy((xf[r] / scales[r]).astype(np.float32)).to(torch.float8_e4m3fn)
+        assert np.array_equal(codes[r], ref.view(torch.uint8).numpy())  # codes, sign of 0 included
+    assert np.all(tab[codes[5]] == 0) and scales[5] == 1.0  # signed zeros keep their sign
+
+
+def pin_fp8_logprob(lib):
+    """FP8 logprob: with inputs that quantise exactly (row amax 448 * 2^-6, values
+    e4m3 integers times 2^-6) it equals the bf16 oracle; on random inputs it equals
+    scipy's log-softmax of the dequantised logits."""
+    rng = np.random.default_rng(42)
+    ints = np.array([0, 1, 2, 3, 4, 5, 6, 7, 8, 16, 32, 448], np.float32)
+    T, H, V = 3, 24, 300
+    hq = rng.choice(ints, (T, H)) * rng.choice([-1, 1], (T, H))
+    wq = rng.choice(ints[:9], (V, H)) * rng.choice([-1, 1], (V, H))
+    hq[:, 0] = 448.0
+    wq[:, 0] = 448.0
+    hb = _bf16_bits((hq * 2.0 ** -6).astype(np.float32))
+    wb = _bf16_bits((wq * 2.0 ** -9).astype(np.float32))
+    tg = rng.integers(0, V, T).astype(np.int32)
+    qh, sh = oracle.quantize_fp8_rows(hb, lib=lib)
+    qw, sw = oracle.quantize_fp8_rows(wb, lib=lib)
+    assert np.all(sh == 2.0 ** -6) and np.all(sw == 2.0 ** -9)
+    a = oracle.logprob_fp8(qh, sh, qw, sw, tg, 0.5, lib=lib)
+    b = oracle.logprob(hb, wb, tg, 0.5, lib=lib)
+    for k in ("logp", "lse", "argmax"):
+        assert np.allclose(a[k], b[k], rtol=1e-14, atol=1e-14), k
+    tab = _e4m3_table()
+    hr = _bf16_bits_round(rng.standard_normal((4, 64)).astype(np.float32))
+    wr = _bf16_bits_round((0.05 * rng.standard_normal((700, 64))).astype(np.float32))
+    qh, sh = oracle.quantize_fp8_rows(hr, lib=lib)
+    qw, sw = oracle.quantize_fp8_rows(wr, lib=lib)
+    tg = rng.integers(0, 700, 4).astype(np.int32)
+    z = (tab[qh] @ tab[qw].T) * sh.astype(np.float64)[:, None] * sw.astype(np.float64)[None, :]
+    r = oracle.logprob_fp8(qh, sh, qw, sw, tg, 1.0, lib=lib)
+    assert np.allclose(r["lse"], scipy.special.logsumexp(z, axis=1), atol=1e-11)
+    assert np.allclose(r["logp"], scipy.special.log_softmax(z, axis=1)[np.arange(4), tg], atol=1e-11)
+    assert np.array_equal(r["argmax"], np.argmax(z, axis=1))
+
+
 PINS = [pin_zero_weights, pin_one_hot_dominant, pin_shift_invariance, pin_temperature,
         pin_brute_force_exact, pin_scipy_logsumexp, pin_ignored_targets,
         pin_block_stats_and_merge, pin_worked_example, pin_stats_closed_forms,
-        pin_backward_finite_differences, pin_backward_closed_forms, pin_entropy]
+        pin_backward_finite_differences, pin_backward_closed_forms, pin_entropy,
+        pin_fp8_quantiser, pin_fp8_logprob]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -413,9 +485,9 @@ def test_pins_catch_planted_mistakes(tmp_path):
     """Each deliberate mistake of oracle.c (ORACLE_MUTANT 1..9: dropped term,
     divided temperature, highest-index ties, LSE without the max, flipped logp
     sign, swapped gap direction, sample variance, backward without inv_temp,
-    unnormalised softmax in the backward, entropy without the LSE shift) fails at
-    least one pin."""
-    for mutant in range(1, 11):
+    unnormalised softmax in the backward, entropy without the LSE shift, fp8
+    rounding up instead of to nearest) fails at least one pin."""
+    for mutant in range(1, 12):
         path = str(tmp_path / f"liboracle_m{mutant}.so")
         oracle.build(path, mutant=mutant)
         lib = oracle.load(path)
