@@ -19,8 +19,8 @@ e2e tokens/s through rlk_logprob with pinned host buffers (H2D of h and
 targets, D2H of logp/lse/argmax inside the timed region; W stays resident as
 model weights do), the dominant kernel's roofline from live CUDA events, SM
 clocks sampled during the timed region, the CPU oracle's throughput on a
-bounded sample, decode-regime points (T = 1..16: HBM-bound) and the backward
-(rlk_logprob_backward on the same batch).
+bounded sample, decode-regime points (T = 1..256: HBM-bound at small T), the
+backward (rlk_logprob_backward on the same batch) and the FP8 (W8A8) variant.
 
 --impl reference times the fp64 CPU oracle (the only reference this method
 has) on the host cores, each step a bounded sample of the same workload.
@@ -57,6 +57,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-backward", action="store_true")
+    p.add_argument("--no-fp8", action="store_true")
     p.add_argument("--decode-only", action="store_true",
                    help="time only the decode regime at T = --decode-T (for profiling)")
     p.add_argument("--decode-T", type=int, default=1)
@@ -329,6 +330,47 @@ def backward_point(rlk, torch, h, W, tg, pk, reps=10):
                 note="flops = 3 x 2*T*H*V (recompute, dz.W, dz^T.h); peak = bf16 burst")
 
 
+def fp8_points(rlk, torch, h, W, tg, pk, reps=20):
+    """The FP8 (W8A8) variant on the same batch: whole rlk_logprob_fp8 call
+    (per-token quantisation of h, e4m3 LM-head kernel, merge) at T=4096 against
+    the fp8 tensor peak (measured bf16 burst x the nominal fp8/bf16 ratio 2), and
+    decode calls streaming the e4m3 weight (V*H bytes) against measured HBM."""
+    T, H = h.shape
+    V = W.shape[0]
+    wq, wsc = rlk.quantize_fp8_rows(W)
+    stream = torch.cuda.current_stream()
+    res = {}
+
+    def timed(hh, tt, n):
+        buf = torch.empty(rlk.fp8_workspace_size(hh.shape[0], H, V), dtype=torch.uint8,
+                          device=h.device)
+        out = [torch.empty(hh.shape[0], device=h.device, dtype=dt)
+               for dt in (torch.float32, torch.float32, torch.int32)]
+        for _ in range(3):
+            rlk.logprob_fp8(hh, wq, wsc, tt, 1.0, workspace=buf, out=out)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            rlk.logprob_fp8(hh, wq, wsc, tt, 1.0, workspace=buf, out=out)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n * 1e-3
+
+    t = timed(h, tg, reps)
+    peak8 = 2.0 * pk["bf16_tflops"]
+    fl = 2.0 * T * H * V
+    res["forward_T4096"] = dict(tokens_per_s=T / t, ms_per_call=t * 1e3, tflops=fl / t / 1e12,
+                                peak_tflops=peak8, frac=fl / t / 1e12 / peak8,
+                                peak_note="fp8 peak = measured bf16 burst x 2 (nominal ratio)")
+    for Td in (1, 16):
+        td = timed(h[:Td].contiguous(), tg[:Td].contiguous(), 50)
+        res[f"decode_T{Td}"] = dict(tokens_per_s=Td / td, us_per_call=td * 1e6,
+                                     hbm_gbs=V * H / td / 1e9, hbm_frac=V * H / td / 1e9 / pk["hbm_gbs"])
+    rlk.check_device_error()
+    return res
+
+
 def run_decode_only(args):
     """Decode regime alone (T = --decode-T rows per call, H=4096, V=151936): used
     for profiling the weight-streaming regime; prints one JSON line."""
@@ -449,6 +491,9 @@ def run_ours(args):
     backward = None
     if not args.no_backward:
         backward = backward_point(rlk, torch, h, W, tg, pk)
+    fp8 = None
+    if not args.no_fp8:
+        fp8 = fp8_points(rlk, torch, h, W, tg, pk)
 
     if rank != 0:
         return 0
@@ -482,7 +527,8 @@ def run_ours(args):
                 clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"],
                             reasons=clk["reasons"], samples=clk["samples"],
                             window=clk.get("window")),
-                decode=decode, backward=backward, bitwise_mismatch_vs_first_call=mism)
+                decode=decode, backward=backward, fp8=fp8,
+                bitwise_mismatch_vs_first_call=mism)
     print(json.dumps(line), flush=True)
     return 0
 

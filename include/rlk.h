@@ -195,6 +195,36 @@ rlk_status rlk_lse_merge_sharded(const rlk_partial *partials, int64_t num_shards
                                  int32_t *out_argmax_i32, rlk_stream_t stream);
 
 /*
+ * FP8 (W8A8) variant.  The consistency blog's dense layers run as FP8 W8A8
+ * GEMMs on inputs quantised with round-to-nearest-even, one fixed accumulation
+ * order per output ("Finish RL Training Faster: Bitwise-Consistent,
+ * High-Performance, Agent-Driven", dense-GEMM and expert-GEMM sections).  Here:
+ * one fp32 scale per row (per token of h, per vocabulary row of W),
+ * s = amax / 448 (1 for an all-zero row), code = e4m3 RNE of x / s (fp32
+ * division, saturating at +-448); z = ((acc * s_h) * s_W) * inv_temp with acc
+ * the fp32 tensor-core sum of code products (tcgen05 kind::f8f6f4, the same
+ * fixed 128 x 256 tiles and K order, now 128 elements per stage).  Row results
+ * keep the batch-invariance contract of rlk_logprob.
+ *
+ * rlk_quantize_fp8_rows: quantise x_bf16 [rows][H] (16-byte aligned) into
+ *   codes [rows][H] (e4m3 bytes, 16-byte aligned) and scales [rows] f32.
+ *   H % 16 == 0.  Asynchronous.  Use it once for W.
+ * rlk_logprob_fp8: quantise h per row into the workspace, then the fp8 LM-head
+ *   kernel and the fixed-tree merge.  weight_e4m3 [V][H] and weight_scales_f32
+ *   [V] as produced by rlk_quantize_fp8_rows; workspace >=
+ *   rlk_logprob_fp8_workspace_size(T, H, V), 16-byte aligned.  Other arguments
+ *   and outputs as rlk_logprob_ws; H % 16 == 0 (else RLK_ERR_ALIGNMENT).
+ */
+rlk_status rlk_quantize_fp8_rows(const void *x_bf16, int64_t rows, int64_t H, uint8_t *codes,
+                                 float *scales, rlk_stream_t stream);
+size_t rlk_logprob_fp8_workspace_size(int64_t T, int64_t H, int64_t V);
+rlk_status rlk_logprob_fp8(const void *hidden_bf16, const uint8_t *weight_e4m3,
+                           const float *weight_scales_f32, const int32_t *targets_i32, int64_t T,
+                           int64_t H, int64_t V, float inv_temp, float *out_logp_f32,
+                           float *out_lse_f32, int32_t *out_argmax_i32, void *workspace,
+                           size_t workspace_bytes, rlk_stream_t stream);
+
+/*
  * rlk_logprob plus the per-token entropy of the softmax over the whole
  * vocabulary, entropy[t] = -sum_v p[t][v] log p[t][v] (the actor-entropy signal
  * reported next to rewards in "Finish RL Training Faster: Bitwise-Consistent,

@@ -20,7 +20,7 @@ __all__ = ["RlkError", "lib", "logprob", "logprob_ws", "logprob_partials", "lse_
            "consistency_stats", "workspace_size", "check_device_error", "vocab_tile", "row_tile",
            "logprob_backward", "backward_workspace_size", "selected_token_logprob",
            "logprob_entropy", "entropy_workspace_size", "logprob_partials_shard",
-           "lse_merge_sharded",
+           "lse_merge_sharded", "quantize_fp8_rows", "logprob_fp8", "fp8_workspace_size",
            "header_functions", "STAT_NAMES", "LIB_PATH", "HEADER_PATH"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -86,6 +86,12 @@ def lib() -> ctypes.CDLL:
         L.rlk_logprob_partials_shard.argtypes = [P, P, P, i64, i64, i64, i64, i64, f32, P, sz, P]
         L.rlk_lse_merge_sharded.restype = st
         L.rlk_lse_merge_sharded.argtypes = [P, i64, i64, P, i64, i64, P, P, P, P]
+        L.rlk_quantize_fp8_rows.restype = st
+        L.rlk_quantize_fp8_rows.argtypes = [P, i64, i64, P, P, P]
+        L.rlk_logprob_fp8_workspace_size.restype = sz
+        L.rlk_logprob_fp8_workspace_size.argtypes = [i64, i64, i64]
+        L.rlk_logprob_fp8.restype = st
+        L.rlk_logprob_fp8.argtypes = [P, P, P, P, i64, i64, i64, f32, P, P, P, P, sz, P]
         L.rlk_logprob_entropy_workspace_size.restype = sz
         L.rlk_logprob_entropy_workspace_size.argtypes = [i64, i64, i64]
         L.rlk_logprob_entropy.restype = st
@@ -373,4 +379,44 @@ def lse_merge_sharded(partials, targets, V: int, out=None, stream=None):
     _check(lib().rlk_lse_merge_sharded(_ptr(partials), R, nvt_s, _ptr(targets), T, int(V),
                                        _ptr(lp), _ptr(lse), _ptr(am), _stream(stream)),
            "rlk_lse_merge_sharded")
+    return lp, lse, am
+
+
+def quantize_fp8_rows(x, stream=None):
+    """rlk_quantize_fp8_rows: bf16 [rows, H] -> (e4m3 codes as uint8 [rows, H], f32 scales [rows])."""
+    import torch
+    _need(x, torch.bfloat16, "x", 2)
+    rows, H = x.shape
+    codes = torch.empty((rows, H), dtype=torch.uint8, device=x.device)
+    scales = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check(lib().rlk_quantize_fp8_rows(_ptr(x), rows, H, _ptr(codes), _ptr(scales),
+                                       _stream(stream)), "rlk_quantize_fp8_rows")
+    return codes, scales
+
+
+def fp8_workspace_size(T: int, H: int, V: int) -> int:
+    return lib().rlk_logprob_fp8_workspace_size(int(T), int(H), int(V))
+
+
+def logprob_fp8(h, W_codes, W_scales, targets, inv_temp: float = 1.0, workspace=None, out=None,
+                stream=None):
+    """rlk_logprob_fp8: (logp, lse, argmax) from bf16 h and an e4m3-quantised W."""
+    import torch
+    _need(h, torch.bfloat16, "h", 2)
+    _need(W_codes, torch.uint8, "W_codes", 2)
+    _need(W_scales, torch.float32, "W_scales", 1)
+    _need(targets, torch.int32, "targets", 1)
+    T, H = h.shape
+    V = W_codes.shape[0]
+    if W_codes.shape[1] != H or W_scales.shape[0] != V or targets.shape[0] != T:
+        raise ValueError("shape mismatch: h [T,H], W_codes [V,H], W_scales [V], targets [T]")
+    lp, lse, am = _outputs(T, h.device, out)
+    if workspace is None:
+        workspace = torch.empty(max(1, fp8_workspace_size(T, H, V)), dtype=torch.uint8,
+                                device=h.device)
+    _need(workspace, torch.uint8, "workspace", 1)
+    _check(lib().rlk_logprob_fp8(_ptr(h), _ptr(W_codes), _ptr(W_scales), _ptr(targets), T, H, V,
+                                 ctypes.c_float(inv_temp), _ptr(lp), _ptr(lse), _ptr(am),
+                                 _ptr(workspace), workspace.numel(), _stream(stream)),
+           "rlk_logprob_fp8")
     return lp, lse, am

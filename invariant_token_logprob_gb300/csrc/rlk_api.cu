@@ -100,20 +100,28 @@ EncodeTiledFn encode_fn() {
     return g_encode;
 }
 
-// 2-D bf16 tensor map over a row-major [rows][cols] matrix, box {kKBlock, box_rows},
-// 128-byte swizzle, zero fill outside the matrix.
-bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
-                    int box_rows) {
+// 2-D tensor map over a row-major [rows][cols] matrix whose boxes are 128 bytes
+// wide (one swizzle row) and box_rows high, 128-byte swizzle, zero fill outside
+// the matrix: bf16 (64 elements per box row) or 8-bit codes (128 elements).
+bool encode_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
+               bool bytes) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
+    const int esize = bytes ? 1 : 2;
     const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
-    const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
-    const cuuint32_t box[2] = {cuuint32_t(kKBlock), cuuint32_t(box_rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols) * esize};
+    const cuuint32_t box[2] = {cuuint32_t(128 / esize), cuuint32_t(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = enc(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                    int box_rows) {
+    return encode_2d(map, base, rows, cols, box_rows, false);
 }
 
 int64_t num_vocab_tiles(int64_t V) { return (V + kVocabTile - 1) / kVocabTile; }
@@ -346,6 +354,66 @@ rlk_status rlk_lse_merge_sharded(const rlk_partial* partials, int64_t num_shards
     return from_cuda(rlk::launch_lse_merge_sharded(partials, int(tiles_per_shard), targets_i32, T,
                                                    V, out_logp_f32, out_lse_f32, out_argmax_i32,
                                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rlk_status rlk_quantize_fp8_rows(const void* x_bf16, int64_t rows, int64_t H, uint8_t* codes,
+                                 float* scales, rlk_stream_t stream) {
+    if (rows < 0 || H < 1 || H > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    if (rows == 0) return RLK_OK;
+    if (!x_bf16 || !codes || !scales) return RLK_ERR_INVALID_ARG;
+    if (H % 16 != 0 || !aligned16(x_bf16) || !aligned16(codes) || !aligned4(scales))
+        return RLK_ERR_ALIGNMENT;
+    int dev, sms;
+    rlk_status st = current_device(&dev, &sms);
+    if (st != RLK_OK) return st;
+    return from_cuda(rlk::launch_quantize_fp8_rows(x_bf16, rows, rows, H, codes, scales,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+int64_t fp8_h_rows(int64_t T) { return T < rlk::kMinTmaRows ? rlk::kMinTmaRows : T; }
+size_t round16(size_t b) { return (b + 15) / 16 * 16; }
+}  // namespace
+
+size_t rlk_logprob_fp8_workspace_size(int64_t T, int64_t H, int64_t V) {
+    if (T <= 0 || V <= 0 || H <= 0) return 0;
+    const size_t rows = size_t(fp8_h_rows(T));
+    return partial_bytes(T, V) + round16(rows * size_t(H)) + round16(rows * 4);
+}
+
+rlk_status rlk_logprob_fp8(const void* hidden_bf16, const uint8_t* weight_e4m3,
+                           const float* weight_scales_f32, const int32_t* targets_i32, int64_t T,
+                           int64_t H, int64_t V, float inv_temp, float* out_logp_f32,
+                           float* out_lse_f32, int32_t* out_argmax_i32, void* workspace,
+                           size_t workspace_bytes, rlk_stream_t stream) {
+    rlk_status st = check_shape(T, H, V, inv_temp);
+    if (st != RLK_OK) return st;
+    if (T == 0) return RLK_OK;
+    if ((st = check_operands(hidden_bf16, weight_e4m3, targets_i32, H)) != RLK_OK) return st;
+    if (!weight_scales_f32) return RLK_ERR_INVALID_ARG;
+    if (H % 16 != 0 || !aligned4(weight_scales_f32)) return RLK_ERR_ALIGNMENT;
+    if ((st = check_outputs(out_logp_f32, out_lse_f32, out_argmax_i32)) != RLK_OK) return st;
+    if (!workspace) return RLK_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return RLK_ERR_ALIGNMENT;
+    if (workspace_bytes < rlk_logprob_fp8_workspace_size(T, H, V)) return RLK_ERR_WORKSPACE;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t hrows = fp8_h_rows(T);
+    char* base = static_cast<char*>(workspace);
+    uint8_t* qh = reinterpret_cast<uint8_t*>(base + partial_bytes(T, V));
+    float* sh = reinterpret_cast<float*>(base + partial_bytes(T, V) + round16(size_t(hrows) * H));
+    cudaError_t e = rlk::launch_quantize_fp8_rows(hidden_bf16, T, hrows, H, qh, sh, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    CUtensorMap th, tw;
+    if (!encode_2d(&th, qh, hrows, H, kRowTile, true) ||
+        !encode_2d(&tw, weight_e4m3, V, H, kVocabTile, true))
+        return RLK_ERR_CUDA;
+    e = rlk::launch_lmhead_partials_fp8(&th, &tw, targets_i32, sh, weight_scales_f32, workspace, T,
+                                        V, H, inv_temp, sms, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(rlk::launch_lse_merge(workspace, targets_i32, T, V, out_logp_f32, out_lse_f32,
+                                           out_argmax_i32, s));
 }
 
 size_t rlk_logprob_entropy_workspace_size(int64_t T, int64_t H, int64_t V) {

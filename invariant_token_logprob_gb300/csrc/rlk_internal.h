@@ -54,6 +54,18 @@ cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, int
                                float* grad_W, bool accumulate_W, cudaStream_t stream);
 void release_backward_handles();
 
+// FP8 (e4m3) operands: th / tw map uint8 codes with boxes {2*kKBlock, rows};
+// sh [rows of th] and sw [V] are the per-row scales; forward partials.
+cudaError_t launch_lmhead_partials_fp8(const CUtensorMap* th, const CUtensorMap* tw,
+                                       const int32_t* targets, const float* sh, const float* sw,
+                                       void* partials, int64_t T, int64_t V, int64_t H,
+                                       float inv_temp, int num_sms, cudaStream_t stream);
+
+// Per-row e4m3 quantisation of bf16 x [rows][H] into codes [out_rows][H] and
+// scales [out_rows]; rows >= `rows` are zero codes with scale 1.  H % 16 == 0.
+cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_rows, int64_t H,
+                                     void* codes, float* scales, cudaStream_t stream);
+
 // Bounded-wait self-test: the forward kernel with its producer issuing no
 // copies, so the MMA warp's wait runs out (kernel error word bit 0) after its
 // time limit and every role returns.

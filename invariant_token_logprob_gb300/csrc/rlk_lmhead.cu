@@ -79,6 +79,8 @@ struct Args {
     int num_tiles;
     float inv_temp;
     int stall_selftest;  // 1: the producer issues no copies (bounded-wait self-test)
+    const float* sh;     // fp8 operands: per-row scale of h [rows]
+    const float* sw;     // fp8 operands: per-row scale of W [V] (this launch's rows)
 };
 
 // Raster: bands of `band` row tiles; inside a band, vocabulary tile outer and
@@ -136,10 +138,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int kMode>
+// kFp8: e4m3 operands (tcgen05 kind::f8f6f4, K = 32 per MMA, 128 K-elements
+// per 128-byte stage row) with per-row scales of h and W applied to the fp32
+// accumulator in the epilogue: z = ((acc * s_h[row]) * s_W[col]) * inv_temp.
+template <int kMode, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmap_h,
                   const __grid_constant__ CUtensorMap tmap_w, const Args p) {
+    static_assert(!kFp8 || kMode == kModePartials, "fp8 operands: forward partials only");
+    constexpr int kBKE = kFp8 ? 2 * kBK : kBK;  // K elements per stage (128 bytes per row)
+    constexpr uint32_t kIdescT = kFp8 ? idesc_e4m3_f32(kBM, kBN) : kIdesc;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -209,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-                    tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage), kb * kBK, m * kBM);
-                    tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), kb * kBK, n * kBN);
+                    tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage), kb * kBKE, m * kBM);
+                    tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), kb * kBKE, n * kBN);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -245,11 +253,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage));
                     const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage));
 #pragma unroll
-                    for (int kk = 0; kk < kBK / kUK; ++kk) {
+                    for (int kk = 0; kk < 4; ++kk) {
+                        // each MMA consumes 32 bytes of every row (16 bf16 or 32 e4m3):
                         // advance the start address by kk * 32 bytes inside the swizzle row
-                        const uint64_t off = uint64_t((kk * kUK * 2) >> 4);
-                        umma_bf16(d_tmem, a_desc + off, b_desc + off, kIdesc,
-                                  (kb | kk) != 0 ? 1u : 0u);
+                        const uint64_t off = uint64_t((kk * 32) >> 4);
+                        if constexpr (kFp8)
+                            umma_f8(d_tmem, a_desc + off, b_desc + off, kIdescT,
+                                    (kb | kk) != 0 ? 1u : 0u);
+                        else
+                            umma_bf16(d_tmem, a_desc + off, b_desc + off, kIdescT,
+                                      (kb | kk) != 0 ? 1u : 0u);
                     }
                     umma_commit(empty_bar(stage));  // frees the smem stage when these MMAs finish
                     if (++stage == kStages) {
@@ -294,15 +307,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float run_m = -INFINITY, run_s = 0.0f, zt = 0.0f;
                 int32_t run_a = INT_MAX;
                 float run_u = 0.0f;  // mode 2 only
+                float row_scale = 1.0f;
+                if constexpr (kFp8) row_scale = row < p.T ? __ldg(p.sh + row) : 0.0f;
                 const uint32_t t_addr = lane_base + acc * uint32_t(kBN);
                 for (int c = 0; c < nchunks; ++c) {
                     uint32_t r[32];
                     tmem_ld32(t_addr + uint32_t(c * 32), r);
                     tmem_ld_wait();
                     float z[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r[j]) * inv_temp;
                     const int nvalid = ncols - c * 32;
+                    if constexpr (kFp8) {
+                        const float* swc = p.sw + col0 + c * 32;  // this launch's W rows
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float cs_ = j < nvalid ? __ldg(swc + j) : 0.0f;
+                            z[j] = __fmul_rn(__fmul_rn(__fmul_rn(__uint_as_float(r[j]), row_scale),
+                                                       cs_),
+                                             inv_temp);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r[j]) * inv_temp;
+                    }
                     if (nvalid < 32) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
@@ -409,23 +435,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-int g_configured[3][64];  // per mode and device: dynamic shared memory attribute set
+int g_configured[4][64];  // per kernel variant and device: smem attribute set
 
-template <int kMode>
+template <int kMode, bool kFp8 = false>
 cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, int64_t H,
                         int num_sms, cudaStream_t stream) {
+    constexpr int kVariant = kFp8 ? 3 : kMode;
+    constexpr int kBKE = kFp8 ? 2 * kBK : kBK;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && !g_configured[kMode][dev]) {
-        e = cudaFuncSetAttribute(lmhead_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(kSmemBytes));
+    if (dev >= 0 && dev < 64 && !g_configured[kVariant][dev]) {
+        e = cudaFuncSetAttribute(lmhead_kernel<kMode, kFp8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
         if (e != cudaSuccess) return e;
-        g_configured[kMode][dev] = 1;
+        g_configured[kVariant][dev] = 1;
     }
     a.num_m = int((a.T + kBM - 1) / kBM);
     a.num_n = int((a.V + kBN - 1) / kBN);
-    a.num_kb = int((H + kBK - 1) / kBK);
+    a.num_kb = int((H + kBKE - 1) / kBKE);
     a.band = a.num_m < 32 ? a.num_m : 32;
     a.num_tiles = a.num_m * a.num_n;
     const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
@@ -439,7 +467,7 @@ cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, in
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, lmhead_kernel<kMode>, *th, *tw, a);
+    e = cudaLaunchKernelEx(&cfg, lmhead_kernel<kMode, kFp8>, *th, *tw, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -472,6 +500,21 @@ cudaError_t launch_lmhead_entropy(const CUtensorMap* th, const CUtensorMap* tw,
     a.V = int(V);
     a.inv_temp = inv_temp;
     return launch_mode<kModeEntropy>(th, tw, a, H, num_sms, stream);
+}
+
+cudaError_t launch_lmhead_partials_fp8(const CUtensorMap* th, const CUtensorMap* tw,
+                                       const int32_t* targets, const float* sh, const float* sw,
+                                       void* partials, int64_t T, int64_t V, int64_t H,
+                                       float inv_temp, int num_sms, cudaStream_t stream) {
+    Args a = {};
+    a.targets = targets;
+    a.partials = static_cast<float4*>(partials);
+    a.sh = sh;
+    a.sw = sw;
+    a.T = T;
+    a.V = int(V);
+    a.inv_temp = inv_temp;
+    return launch_mode<kModePartials, true>(th, tw, a, H, num_sms, stream);
 }
 
 cudaError_t launch_lmhead_stall_selftest(const CUtensorMap* th, const CUtensorMap* tw,

@@ -1,0 +1,94 @@
+"""GPU tests of the FP8 (W8A8) LM-head variant.
+
+* Quantisation is integer work: e4m3 codes and fp32 scales must equal the
+  oracle's bit for bit (both take the rounding decision on the same fp32
+  quotient x / s).
+* The logprob is compared with the oracle's fp64 logprob on the same codes and
+  scales, under the parity tolerances of the bf16 path (|dlogp| <= 5e-4,
+  |dlse| <= 1e-5 max(1, |lse|), argmax exact where the top-2 gap > 1e-3): the
+  only difference left is the fp32 accumulation of exact code products.
+* The batch-invariance contract holds for this variant too (bitwise).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_bitwise, assert_parity, to_dev
+from invariant_token_logprob_gb300.inputs import lm_head_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import invariant_token_logprob_gb300 as rlk
+    rlk.lib()
+
+
+def _np(xs):
+    return tuple(x.cpu().numpy() for x in xs)
+
+
+def test_quantiser_codes_and_scales_are_bit_exact(olib):
+    import invariant_token_logprob_gb300 as rlk
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(37, 4096, generator=g) * torch.logspace(-4, 3, 37)[:, None]
+    x[3] = 0.0                                    # all-zero row: scale 1, codes 0
+    x[4, :5] = torch.tensor([448.0, -448.0, 1e-30, 3.0, -0.0])
+    xb = x.to(torch.bfloat16)
+    codes, scales = rlk.quantize_fp8_rows(xb.cuda())
+    torch.cuda.synchronize()
+    rc, rs = oracle.quantize_fp8_rows(xb, lib=olib)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+@pytest.mark.parametrize("T,H,V,seed", [(64, 256, 1024, 1), (3, 64, 777, 2), (130, 512, 3001, 3),
+                                        (2, 4096, 151936, 4)])
+def test_fp8_logprob_matches_oracle(T, H, V, seed, olib):
+    import invariant_token_logprob_gb300 as rlk
+    d = to_dev(lm_head_inputs(T, H, V, seed=seed))
+    it = float(np.float32(1 / 0.7)) if seed % 2 else 1.0
+    wq, ws = rlk.quantize_fp8_rows(d["W"])
+    gpu = _np(rlk.logprob_fp8(d["h"], wq, ws, d["targets"], it))
+    rlk.check_device_error()
+    qh, sh = oracle.quantize_fp8_rows(d["h"].cpu(), lib=olib)
+    qw, sw = oracle.quantize_fp8_rows(d["W"].cpu(), lib=olib)
+    assert np.array_equal(qw, wq.cpu().numpy())
+    ref = oracle.logprob_fp8(qh, sh, qw, sw, d["targets"].cpu(), it, lib=olib)
+    assert_parity(gpu, ref, what=f"fp8 T={T} H={H} V={V}")
+
+
+def test_fp8_batch_invariance_small():
+    import invariant_token_logprob_gb300 as rlk
+    d = to_dev(lm_head_inputs(64, 256, 3000, seed=9))
+    wq, ws = rlk.quantize_fp8_rows(d["W"])
+    full = _np(rlk.logprob_fp8(d["h"], wq, ws, d["targets"]))
+    for c in (1, 5, 16, 17, 63):
+        parts = [_np(rlk.logprob_fp8(d["h"][i:i + c].contiguous(), wq, ws,
+                                     d["targets"][i:i + c].contiguous())) for i in range(0, 64, c)]
+        got = tuple(np.concatenate([p[k] for p in parts]) for k in range(3))
+        assert_bitwise(full, got, f"fp8 chunk={c}")
+
+
+@pytest.mark.slow
+def test_fp8_full_size_parity_and_invariance(olib):
+    import invariant_token_logprob_gb300 as rlk
+    T, H, V = 4096, 4096, 151936
+    d = lm_head_inputs(T, H, V, seed=13, device="cuda")
+    wq, ws = rlk.quantize_fp8_rows(d["W"])
+    full = _np(rlk.logprob_fp8(d["h"], wq, ws, d["targets"]))
+    rows = np.array([0, 1, 1000, 2048, T - 1])
+    hs = d["h"][torch.from_numpy(rows).cuda()].cpu()
+    qh, sh = oracle.quantize_fp8_rows(hs, lib=olib)
+    ref = oracle.logprob_fp8(qh, sh, wq.cpu().numpy(), ws.cpu().numpy(),
+                             d["targets"][torch.from_numpy(rows).cuda()].cpu(), 1.0, lib=olib)
+    assert_parity(tuple(x[rows] for x in full), ref, what="fp8 T=4096")
+    seq = [_np(rlk.logprob_fp8(d["h"][i:i + 512].contiguous(), wq, ws,
+                               d["targets"][i:i + 512].contiguous())) for i in range(0, T, 512)]
+    assert_bitwise(full, tuple(np.concatenate([p[k] for p in seq]) for k in range(3)), "fp8 8x512")
+    one = _np(rlk.logprob_fp8(d["h"][7:8].contiguous(), wq, ws, d["targets"][7:8].contiguous()))
+    assert_bitwise(tuple(x[7:8] for x in full), one, "fp8 T=1 vs T=4096")
