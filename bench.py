@@ -61,6 +61,7 @@ def parse():
     p.add_argument("--decode-only", action="store_true",
                    help="time only the decode regime at T = --decode-T (for profiling)")
     p.add_argument("--decode-T", type=int, default=1)
+    p.add_argument("--fp8", action="store_true", help="decode-only: the FP8 (e4m3 W) variant")
     return p.parse_args()
 
 
@@ -381,8 +382,28 @@ def run_decode_only(args):
     g = torch.Generator(device="cuda").manual_seed(1000)
     W = (torch.randn(V_CFG, H_CFG, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
     stream = torch.cuda.current_stream()
-    res = decode_points(rlk, torch, W, stream, pk, Ts=(args.decode_T,), reps=args.steps,
-                        rounds=1)
+    if args.fp8:
+        T = args.decode_T
+        wq, wsc = rlk.quantize_fp8_rows(W)
+        h = torch.randn(T, H_CFG, device="cuda").to(torch.bfloat16)
+        tg = torch.randint(0, V_CFG, (T,), device="cuda", dtype=torch.int32)
+        buf = torch.empty(rlk.fp8_workspace_size(T, H_CFG, V_CFG), dtype=torch.uint8, device="cuda")
+        out = [torch.empty(T, device="cuda", dtype=dt) for dt in (torch.float32, torch.float32, torch.int32)]
+        for _ in range(3):
+            rlk.logprob_fp8(h, wq, wsc, tg, 1.0, workspace=buf, out=out)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            rlk.logprob_fp8(h, wq, wsc, tg, 1.0, workspace=buf, out=out)
+        e1.record(stream)
+        e1.synchronize()
+        t = e0.elapsed_time(e1) / args.steps * 1e-3
+        res = {f"T{T}_fp8": dict(us_per_call=t * 1e6, hbm_gbs=V_CFG * H_CFG / t / 1e9,
+                                  hbm_frac=V_CFG * H_CFG / t / 1e9 / pk["hbm_gbs"])}
+    else:
+        res = decode_points(rlk, torch, W, stream, pk, Ts=(args.decode_T,), reps=args.steps,
+                            rounds=1)
     rlk.check_device_error()
     print(json.dumps(dict(mode="decode-only", H=H_CFG, V=V_CFG, **res)), flush=True)
     return 0

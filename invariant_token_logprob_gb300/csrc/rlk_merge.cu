@@ -59,8 +59,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     int32_t a = INT_MAX;
     // Lane l folds tiles l, l+32, l+64, ... in ascending order.  The records are
     // fetched kBatch at a time before folding them (same order, same bits), so a
-    // row costs a few memory round trips instead of one per tile.
-    constexpr int kBatch = 8;
+    // row with up to 768 tiles costs one memory round trip instead of one per tile.
+    constexpr int kBatch = 24;
     for (int j0 = lane; j0 < nvt; j0 += 32 * kBatch) {
         float4 q[kBatch];
         float uq[kBatch];

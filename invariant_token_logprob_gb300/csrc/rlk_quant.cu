@@ -6,7 +6,7 @@
 // dense-GEMM and expert-GEMM sections).  Per row r of a bf16 matrix [rows][H]:
 //   s_r  = amax_k |x[r,k]| / 448   (fp32 division; 1 for an all-zero row)
 //   q    = e4m3 RNE of x[r,k] / s_r (fp32 division), saturating at +-448
-// One warp per row; the max is exact whatever the order, the division is the
+// One CTA per row; the max is exact whatever the order, the division is the
 // IEEE one and the conversion is the hardware's RNE cvt, so a row's codes and
 // scale depend only on that row.  Rows out_rows > rows (zero padding for small
 // T) get code 0 and scale 1.
@@ -19,25 +19,28 @@
 namespace rlk {
 namespace {
 
-constexpr int kQuantWarps = 8;
+constexpr int kQuantThreads = 256;
 
-__global__ void __launch_bounds__(kQuantWarps * 32)
-    quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t out_rows,
-                         int H, uint8_t* __restrict__ codes, float* __restrict__ scales) {
+// One CTA per row: the 256 threads share the row's elements, the amax is
+// reduced through warp shuffles and shared memory (a max: exact in any order),
+// and every element is then divided and converted on its own.
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int H,
+                         uint8_t* __restrict__ codes, float* __restrict__ scales) {
     grid_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int64_t r = int64_t(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
-    if (r >= out_rows) return;
+    __shared__ float warp_max[kQuantThreads / 32];
+    const int tid = threadIdx.x;
+    const int64_t r = blockIdx.x;
     uint8_t* cr = codes + r * int64_t(H);
-    if (r >= rows) {
-        for (int k = lane * 16; k < H; k += 32 * 16)
+    if (r >= rows) {  // zero padding rows (uniform per CTA)
+        for (int k = tid * 16; k < H; k += kQuantThreads * 16)
             *reinterpret_cast<uint4*>(cr + k) = make_uint4(0u, 0u, 0u, 0u);
-        if (lane == 0) scales[r] = 1.0f;
+        if (tid == 0) scales[r] = 1.0f;
         return;
     }
     const __nv_bfloat16* xr = x + r * int64_t(H);
     float amax = 0.0f;
-    for (int k = lane * 8; k < H; k += 32 * 8) {  // H % 16 == 0: whole 16-byte vectors
+    for (int k = tid * 8; k < H; k += kQuantThreads * 8) {  // H % 16 == 0
         const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
         const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
@@ -48,8 +51,13 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((tid & 31) == 0) warp_max[tid >> 5] = amax;
+    __syncthreads();
+    amax = warp_max[0];
+#pragma unroll
+    for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
     const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    for (int k = lane * 16; k < H; k += 32 * 16) {
+    for (int k = tid * 16; k < H; k += kQuantThreads * 16) {
         uint32_t out[4];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -68,17 +76,15 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
         }
         *reinterpret_cast<uint4*>(cr + k) = make_uint4(out[0], out[1], out[2], out[3]);
     }
-    if (lane == 0) scales[r] = sc;
+    if (tid == 0) scales[r] = sc;
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_rows, int64_t H,
                                      void* codes, float* scales, cudaStream_t stream) {
-    const int64_t blocks = (out_rows + kQuantWarps - 1) / kQuantWarps;
-    quantize_rows_kernel<<<unsigned(blocks), kQuantWarps * 32, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), rows, out_rows, int(H), static_cast<uint8_t*>(codes),
-        scales);
+    quantize_rows_kernel<<<unsigned(out_rows), kQuantThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, int(H), static_cast<uint8_t*>(codes), scales);
     return cudaGetLastError();
 }
 
