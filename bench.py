@@ -338,7 +338,7 @@ def fp8_points(rlk, torch, h, W, tg, pk, reps=20):
     decode calls streaming the e4m3 weight (V*H bytes) against measured HBM."""
     T, H = h.shape
     V = W.shape[0]
-    wq, wsc = rlk.quantize_fp8_rows(W)
+    wq, wsc = rlk.quantize_fp8_weight(W)
     stream = torch.cuda.current_stream()
     res = {}
 
@@ -384,7 +384,7 @@ def run_decode_only(args):
     stream = torch.cuda.current_stream()
     if args.fp8:
         T = args.decode_T
-        wq, wsc = rlk.quantize_fp8_rows(W)
+        wq, wsc = rlk.quantize_fp8_weight(W)
         h = torch.randn(T, H_CFG, device="cuda").to(torch.bfloat16)
         tg = torch.randint(0, V_CFG, (T,), device="cuda", dtype=torch.int32)
         buf = torch.empty(rlk.fp8_workspace_size(T, H_CFG, V_CFG), dtype=torch.uint8, device="cuda")

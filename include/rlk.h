@@ -207,16 +207,29 @@ rlk_status rlk_lse_merge_sharded(const rlk_partial *partials, int64_t num_shards
  * keep the batch-invariance contract of rlk_logprob.
  *
  * rlk_quantize_fp8_rows: quantise x_bf16 [rows][H] (16-byte aligned) into
- *   codes [rows][H] (e4m3 bytes, 16-byte aligned) and scales [rows] f32.
- *   H % 16 == 0.  Asynchronous.  Use it once for W.
+ *   row-major codes [rows][H] (e4m3 bytes, 16-byte aligned) and scales [rows]
+ *   f32.  H % 16 == 0.  Asynchronous.  (What rlk_logprob_fp8 does to h.)
+ * rlk_quantize_fp8_weight: the same quantisation of W [V][H] written in the
+ *   tile-packed fp8 weight format: rows grouped in vocabulary tiles of
+ *   rlk_vocab_tile() rows (the last tile padded with zero codes), columns in
+ *   128-byte k-blocks, and each (tile j, k-block b) stored as one contiguous
+ *   block of rlk_vocab_tile() x 128 bytes at ((j * H/128 + b) * rlk_vocab_tile()
+ *   + row % rlk_vocab_tile()) * 128 + column % 128.  Every weight read of the
+ *   kernel is then one contiguous 32 KB block (reading 4 KB-long rows 128 bytes
+ *   at a time streamed at only ~4.5 TB/s on GB300).  packed_e4m3 holds
+ *   rlk_fp8_weight_bytes(V, H) bytes, scales V floats.  H % 128 == 0.
+ *   Asynchronous; run once per weight update.
  * rlk_logprob_fp8: quantise h per row into the workspace, then the fp8 LM-head
- *   kernel and the fixed-tree merge.  weight_e4m3 [V][H] and weight_scales_f32
- *   [V] as produced by rlk_quantize_fp8_rows; workspace >=
+ *   kernel and the fixed-tree merge.  weight_e4m3 / weight_scales_f32 as
+ *   produced by rlk_quantize_fp8_weight; workspace >=
  *   rlk_logprob_fp8_workspace_size(T, H, V), 16-byte aligned.  Other arguments
- *   and outputs as rlk_logprob_ws; H % 16 == 0 (else RLK_ERR_ALIGNMENT).
+ *   and outputs as rlk_logprob_ws; H % 128 == 0 (else RLK_ERR_ALIGNMENT).
  */
 rlk_status rlk_quantize_fp8_rows(const void *x_bf16, int64_t rows, int64_t H, uint8_t *codes,
                                  float *scales, rlk_stream_t stream);
+size_t rlk_fp8_weight_bytes(int64_t V, int64_t H);
+rlk_status rlk_quantize_fp8_weight(const void *weight_bf16, int64_t V, int64_t H,
+                                   uint8_t *packed_e4m3, float *scales, rlk_stream_t stream);
 size_t rlk_logprob_fp8_workspace_size(int64_t T, int64_t H, int64_t V);
 rlk_status rlk_logprob_fp8(const void *hidden_bf16, const uint8_t *weight_e4m3,
                            const float *weight_scales_f32, const int32_t *targets_i32, int64_t T,

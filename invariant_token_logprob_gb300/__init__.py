@@ -21,6 +21,7 @@ __all__ = ["RlkError", "lib", "logprob", "logprob_ws", "logprob_partials", "lse_
            "logprob_backward", "backward_workspace_size", "selected_token_logprob",
            "logprob_entropy", "entropy_workspace_size", "logprob_partials_shard",
            "lse_merge_sharded", "quantize_fp8_rows", "logprob_fp8", "fp8_workspace_size",
+           "quantize_fp8_weight", "unpack_fp8_weight",
            "header_functions", "STAT_NAMES", "LIB_PATH", "HEADER_PATH"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -88,6 +89,10 @@ def lib() -> ctypes.CDLL:
         L.rlk_lse_merge_sharded.argtypes = [P, i64, i64, P, i64, i64, P, P, P, P]
         L.rlk_quantize_fp8_rows.restype = st
         L.rlk_quantize_fp8_rows.argtypes = [P, i64, i64, P, P, P]
+        L.rlk_fp8_weight_bytes.restype = sz
+        L.rlk_fp8_weight_bytes.argtypes = [i64, i64]
+        L.rlk_quantize_fp8_weight.restype = st
+        L.rlk_quantize_fp8_weight.argtypes = [P, i64, i64, P, P, P]
         L.rlk_logprob_fp8_workspace_size.restype = sz
         L.rlk_logprob_fp8_workspace_size.argtypes = [i64, i64, i64]
         L.rlk_logprob_fp8.restype = st
@@ -398,24 +403,46 @@ def fp8_workspace_size(T: int, H: int, V: int) -> int:
     return lib().rlk_logprob_fp8_workspace_size(int(T), int(H), int(V))
 
 
-def logprob_fp8(h, W_codes, W_scales, targets, inv_temp: float = 1.0, workspace=None, out=None,
+def quantize_fp8_weight(W, stream=None):
+    """rlk_quantize_fp8_weight: bf16 W [V, H] -> (tile-packed e4m3 codes as a flat uint8
+    tensor, f32 scales [V])."""
+    import torch
+    _need(W, torch.bfloat16, "W", 2)
+    V, H = W.shape
+    packed = torch.empty(lib().rlk_fp8_weight_bytes(V, H), dtype=torch.uint8, device=W.device)
+    scales = torch.empty(V, dtype=torch.float32, device=W.device)
+    _check(lib().rlk_quantize_fp8_weight(_ptr(W), V, H, _ptr(packed), _ptr(scales),
+                                         _stream(stream)), "rlk_quantize_fp8_weight")
+    return packed, scales
+
+
+def unpack_fp8_weight(packed, V: int, H: int):
+    """Row-major [V, H] copy of a tile-packed fp8 weight (for inspection)."""
+    bn = vocab_tile()
+    nt = (V + bn - 1) // bn
+    x = packed.view(nt, H // 128, bn, 128).permute(0, 2, 1, 3).reshape(nt * bn, H)
+    return x[:V]
+
+
+def logprob_fp8(h, W_packed, W_scales, targets, inv_temp: float = 1.0, workspace=None, out=None,
                 stream=None):
-    """rlk_logprob_fp8: (logp, lse, argmax) from bf16 h and an e4m3-quantised W."""
+    """rlk_logprob_fp8: (logp, lse, argmax) from bf16 h and a tile-packed e4m3 W
+    (from quantize_fp8_weight); V = len(W_scales)."""
     import torch
     _need(h, torch.bfloat16, "h", 2)
-    _need(W_codes, torch.uint8, "W_codes", 2)
+    _need(W_packed, torch.uint8, "W_packed", 1)
     _need(W_scales, torch.float32, "W_scales", 1)
     _need(targets, torch.int32, "targets", 1)
     T, H = h.shape
-    V = W_codes.shape[0]
-    if W_codes.shape[1] != H or W_scales.shape[0] != V or targets.shape[0] != T:
-        raise ValueError("shape mismatch: h [T,H], W_codes [V,H], W_scales [V], targets [T]")
+    V = W_scales.shape[0]
+    if W_packed.numel() < lib().rlk_fp8_weight_bytes(V, H) or targets.shape[0] != T:
+        raise ValueError("W_packed must hold rlk_fp8_weight_bytes(V, H) bytes; targets [T]")
     lp, lse, am = _outputs(T, h.device, out)
     if workspace is None:
         workspace = torch.empty(max(1, fp8_workspace_size(T, H, V)), dtype=torch.uint8,
                                 device=h.device)
     _need(workspace, torch.uint8, "workspace", 1)
-    _check(lib().rlk_logprob_fp8(_ptr(h), _ptr(W_codes), _ptr(W_scales), _ptr(targets), T, H, V,
+    _check(lib().rlk_logprob_fp8(_ptr(h), _ptr(W_packed), _ptr(W_scales), _ptr(targets), T, H, V,
                                  ctypes.c_float(inv_temp), _ptr(lp), _ptr(lse), _ptr(am),
                                  _ptr(workspace), workspace.numel(), _stream(stream)),
            "rlk_logprob_fp8")

@@ -375,6 +375,24 @@ int64_t fp8_h_rows(int64_t T) { return T < rlk::kMinTmaRows ? rlk::kMinTmaRows :
 size_t round16(size_t b) { return (b + 15) / 16 * 16; }
 }  // namespace
 
+size_t rlk_fp8_weight_bytes(int64_t V, int64_t H) {
+    if (V <= 0 || H <= 0) return 0;
+    return size_t(num_vocab_tiles(V)) * size_t(kVocabTile) * size_t(H);
+}
+
+rlk_status rlk_quantize_fp8_weight(const void* weight_bf16, int64_t V, int64_t H,
+                                   uint8_t* packed_e4m3, float* scales, rlk_stream_t stream) {
+    if (V < 1 || V > INT32_MAX || H < 1 || H > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    if (!weight_bf16 || !packed_e4m3 || !scales) return RLK_ERR_INVALID_ARG;
+    if (H % 128 != 0 || !aligned16(weight_bf16) || !aligned16(packed_e4m3) || !aligned4(scales))
+        return RLK_ERR_ALIGNMENT;
+    int dev, sms;
+    rlk_status st = current_device(&dev, &sms);
+    if (st != RLK_OK) return st;
+    return from_cuda(rlk::launch_quantize_fp8_weight_tiled(weight_bf16, V, H, packed_e4m3, scales,
+                                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t rlk_logprob_fp8_workspace_size(int64_t T, int64_t H, int64_t V) {
     if (T <= 0 || V <= 0 || H <= 0) return 0;
     const size_t rows = size_t(fp8_h_rows(T));
@@ -391,7 +409,7 @@ rlk_status rlk_logprob_fp8(const void* hidden_bf16, const uint8_t* weight_e4m3,
     if (T == 0) return RLK_OK;
     if ((st = check_operands(hidden_bf16, weight_e4m3, targets_i32, H)) != RLK_OK) return st;
     if (!weight_scales_f32) return RLK_ERR_INVALID_ARG;
-    if (H % 16 != 0 || !aligned4(weight_scales_f32)) return RLK_ERR_ALIGNMENT;
+    if (H % 128 != 0 || !aligned4(weight_scales_f32)) return RLK_ERR_ALIGNMENT;
     if ((st = check_outputs(out_logp_f32, out_lse_f32, out_argmax_i32)) != RLK_OK) return st;
     if (!workspace) return RLK_ERR_WORKSPACE;
     if (!aligned16(workspace)) return RLK_ERR_ALIGNMENT;
@@ -406,8 +424,10 @@ rlk_status rlk_logprob_fp8(const void* hidden_bf16, const uint8_t* weight_e4m3,
     cudaError_t e = rlk::launch_quantize_fp8_rows(hidden_bf16, T, hrows, H, qh, sh, s);
     if (e != cudaSuccess) return from_cuda(e);
     CUtensorMap th, tw;
+    // the packed weight as rows of 128 bytes: blocks * kVocabTile of them
+    const int64_t packed_rows = num_vocab_tiles(V) * (H / 128) * kVocabTile;
     if (!encode_2d(&th, qh, hrows, H, kRowTile, true) ||
-        !encode_2d(&tw, weight_e4m3, V, H, kVocabTile, true))
+        !encode_2d(&tw, weight_e4m3, packed_rows, 128, kVocabTile, true))
         return RLK_ERR_CUDA;
     e = rlk::launch_lmhead_partials_fp8(&th, &tw, targets_i32, sh, weight_scales_f32, workspace, T,
                                         V, H, inv_temp, sms, s);

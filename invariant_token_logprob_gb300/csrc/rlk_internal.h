@@ -54,7 +54,9 @@ cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, int
                                float* grad_W, bool accumulate_W, cudaStream_t stream);
 void release_backward_handles();
 
-// FP8 (e4m3) operands: th / tw map uint8 codes with boxes {2*kKBlock, rows};
+// FP8 (e4m3) operands: th maps row-major uint8 codes with boxes {2*kKBlock, rows};
+// tw maps the tile-packed weight as [blocks * kVocabTile][128] with boxes
+// {128, kVocabTile} (box (n, kb) at row (n * num_kb + kb) * kVocabTile);
 // sh [rows of th] and sw [V] are the per-row scales; forward partials.
 cudaError_t launch_lmhead_partials_fp8(const CUtensorMap* th, const CUtensorMap* tw,
                                        const int32_t* targets, const float* sh, const float* sw,
@@ -65,6 +67,12 @@ cudaError_t launch_lmhead_partials_fp8(const CUtensorMap* th, const CUtensorMap*
 // scales [out_rows]; rows >= `rows` are zero codes with scale 1.  H % 16 == 0.
 cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_rows, int64_t H,
                                      void* codes, float* scales, cudaStream_t stream);
+
+// Quantise W [V][H] (H % 128 == 0) into the tile-packed fp8 weight format
+// (ceil(V/kVocabTile) * kVocabTile * H bytes; padding rows are zero codes) and
+// scales [V].
+cudaError_t launch_quantize_fp8_weight_tiled(const void* W, int64_t V, int64_t H, void* packed,
+                                             float* scales, cudaStream_t stream);
 
 // Bounded-wait self-test: the forward kernel with its producer issuing no
 // copies, so the MMA warp's wait runs out (kernel error word bit 0) after its

@@ -218,7 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
                     tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage), kb * kBKE, m * kBM);
-                    tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), kb * kBKE, n * kBN);
+                    if constexpr (kFp8)  // tile-packed weight: one contiguous 32 KB block
+                        tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), 0,
+                                    (n * p.num_kb + kb) * kBN);
+                    else
+                        tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), kb * kBKE, n * kBN);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;

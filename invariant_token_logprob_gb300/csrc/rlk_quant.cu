@@ -24,18 +24,37 @@ constexpr int kQuantThreads = 256;
 // One CTA per row: the 256 threads share the row's elements, the amax is
 // reduced through warp shuffles and shared memory (a max: exact in any order),
 // and every element is then divided and converted on its own.
+// Byte offset of code (row r, column k) in the output.  Row-major: r*H + k.
+// Tile-packed (the fp8 weight format): rows grouped in vocabulary tiles of
+// kVocabTile, columns in 128-byte k-blocks, each (tile, k-block) a contiguous
+// kVocabTile x 128-byte block: ((tile * nkb + kb) * kVocabTile + r % kVocabTile)
+// * 128 + k % 128.  Every TMA box of the LM-head kernel is then one contiguous
+// 32 KB read instead of 256 strided 128-byte pieces.
+template <bool kTiled>
+__device__ __forceinline__ int64_t code_offset(int64_t r, int k, int H) {
+    if constexpr (kTiled) {
+        const int nkb = H / 128;
+        const int64_t tile = r / kVocabTile;
+        return ((tile * nkb + k / 128) * kVocabTile + r % kVocabTile) * 128 + k % 128;
+    } else {
+        return r * int64_t(H) + k;
+    }
+}
+
+template <bool kTiled>
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int H,
-                         uint8_t* __restrict__ codes, float* __restrict__ scales) {
+                         uint8_t* __restrict__ codes, float* __restrict__ scales,
+                         int64_t scale_rows) {
     grid_launch_dependents();
     __shared__ float warp_max[kQuantThreads / 32];
     const int tid = threadIdx.x;
     const int64_t r = blockIdx.x;
-    uint8_t* cr = codes + r * int64_t(H);
     if (r >= rows) {  // zero padding rows (uniform per CTA)
         for (int k = tid * 16; k < H; k += kQuantThreads * 16)
-            *reinterpret_cast<uint4*>(cr + k) = make_uint4(0u, 0u, 0u, 0u);
-        if (tid == 0) scales[r] = 1.0f;
+            *reinterpret_cast<uint4*>(codes + code_offset<kTiled>(r, k, H)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        if (tid == 0 && r < scale_rows) scales[r] = 1.0f;
         return;
     }
     const __nv_bfloat16* xr = x + r * int64_t(H);
@@ -74,7 +93,8 @@ __global__ void __launch_bounds__(kQuantThreads)
                 out[half * 2 + i / 2] = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
             }
         }
-        *reinterpret_cast<uint4*>(cr + k) = make_uint4(out[0], out[1], out[2], out[3]);
+        *reinterpret_cast<uint4*>(codes + code_offset<kTiled>(r, k, H)) =
+            make_uint4(out[0], out[1], out[2], out[3]);
     }
     if (tid == 0) scales[r] = sc;
 }
@@ -83,8 +103,17 @@ __global__ void __launch_bounds__(kQuantThreads)
 
 cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_rows, int64_t H,
                                      void* codes, float* scales, cudaStream_t stream) {
-    quantize_rows_kernel<<<unsigned(out_rows), kQuantThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), rows, int(H), static_cast<uint8_t*>(codes), scales);
+    quantize_rows_kernel<false><<<unsigned(out_rows), kQuantThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, int(H), static_cast<uint8_t*>(codes), scales,
+        out_rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp8_weight_tiled(const void* W, int64_t V, int64_t H, void* packed,
+                                             float* scales, cudaStream_t stream) {
+    const int64_t padded = (V + kVocabTile - 1) / kVocabTile * kVocabTile;
+    quantize_rows_kernel<true><<<unsigned(padded), kQuantThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(W), V, int(H), static_cast<uint8_t*>(packed), scales, V);
     return cudaGetLastError();
 }
 

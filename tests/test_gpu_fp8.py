@@ -46,18 +46,34 @@ def test_quantiser_codes_and_scales_are_bit_exact(olib):
     assert np.array_equal(codes.cpu().numpy(), rc)
 
 
-@pytest.mark.parametrize("T,H,V,seed", [(64, 256, 1024, 1), (3, 64, 777, 2), (130, 512, 3001, 3),
+def test_packed_weight_codes_are_bit_exact_and_padded_with_zeros(olib):
+    """The tile-packed fp8 weight holds the oracle's row codes (after unpacking)
+    and zero codes in the padding rows of the last vocabulary tile."""
+    import invariant_token_logprob_gb300 as rlk
+    V, H = 1000, 384
+    W = (torch.randn(V, H, generator=torch.Generator().manual_seed(6)) * 0.02).to(torch.bfloat16)
+    packed, scales = rlk.quantize_fp8_weight(W.cuda())
+    torch.cuda.synchronize()
+    assert packed.numel() == 1024 * H
+    rc, rs = oracle.quantize_fp8_rows(W, lib=olib)
+    assert np.array_equal(rlk.unpack_fp8_weight(packed, V, H).cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    full = rlk.unpack_fp8_weight(packed, 1024, H)  # including the padding rows
+    assert torch.all(full[V:] == 0)
+
+
+@pytest.mark.parametrize("T,H,V,seed", [(64, 256, 1024, 1), (3, 128, 777, 2), (130, 512, 3001, 3),
                                         (2, 4096, 151936, 4)])
 def test_fp8_logprob_matches_oracle(T, H, V, seed, olib):
     import invariant_token_logprob_gb300 as rlk
     d = to_dev(lm_head_inputs(T, H, V, seed=seed))
     it = float(np.float32(1 / 0.7)) if seed % 2 else 1.0
-    wq, ws = rlk.quantize_fp8_rows(d["W"])
+    wq, ws = rlk.quantize_fp8_weight(d["W"])
     gpu = _np(rlk.logprob_fp8(d["h"], wq, ws, d["targets"], it))
     rlk.check_device_error()
     qh, sh = oracle.quantize_fp8_rows(d["h"].cpu(), lib=olib)
     qw, sw = oracle.quantize_fp8_rows(d["W"].cpu(), lib=olib)
-    assert np.array_equal(qw, wq.cpu().numpy())
+    assert np.array_equal(qw, rlk.unpack_fp8_weight(wq, V, H).cpu().numpy())
     ref = oracle.logprob_fp8(qh, sh, qw, sw, d["targets"].cpu(), it, lib=olib)
     assert_parity(gpu, ref, what=f"fp8 T={T} H={H} V={V}")
 
@@ -65,7 +81,7 @@ def test_fp8_logprob_matches_oracle(T, H, V, seed, olib):
 def test_fp8_batch_invariance_small():
     import invariant_token_logprob_gb300 as rlk
     d = to_dev(lm_head_inputs(64, 256, 3000, seed=9))
-    wq, ws = rlk.quantize_fp8_rows(d["W"])
+    wq, ws = rlk.quantize_fp8_weight(d["W"])
     full = _np(rlk.logprob_fp8(d["h"], wq, ws, d["targets"]))
     for c in (1, 5, 16, 17, 63):
         parts = [_np(rlk.logprob_fp8(d["h"][i:i + c].contiguous(), wq, ws,
@@ -79,12 +95,12 @@ def test_fp8_full_size_parity_and_invariance(olib):
     import invariant_token_logprob_gb300 as rlk
     T, H, V = 4096, 4096, 151936
     d = lm_head_inputs(T, H, V, seed=13, device="cuda")
-    wq, ws = rlk.quantize_fp8_rows(d["W"])
+    wq, ws = rlk.quantize_fp8_weight(d["W"])
     full = _np(rlk.logprob_fp8(d["h"], wq, ws, d["targets"]))
     rows = np.array([0, 1, 1000, 2048, T - 1])
     hs = d["h"][torch.from_numpy(rows).cuda()].cpu()
     qh, sh = oracle.quantize_fp8_rows(hs, lib=olib)
-    ref = oracle.logprob_fp8(qh, sh, wq.cpu().numpy(), ws.cpu().numpy(),
+    ref = oracle.logprob_fp8(qh, sh, rlk.unpack_fp8_weight(wq, V, H).cpu().numpy(), ws.cpu().numpy(),
                              d["targets"][torch.from_numpy(rows).cuda()].cpu(), 1.0, lib=olib)
     assert_parity(tuple(x[rows] for x in full), ref, what="fp8 T=4096")
     seq = [_np(rlk.logprob_fp8(d["h"][i:i + 512].contiguous(), wq, ws,
