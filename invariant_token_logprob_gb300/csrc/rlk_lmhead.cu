@@ -298,6 +298,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_coords(p, tile, m, n);
             const int64_t row = int64_t(m) * kBM + row_in_tile;
             const int32_t tgt = row < p.T ? __ldg(p.targets + row) : -1;
+            // fp8: fetch the tile's 256 column scales now, while the MMAs run --
+            // lane l keeps the scale of column 32*i + l for chunk i -- and the row's.
+            float col_scale[kBN / 32];
+            float row_scale = 1.0f;
+            if constexpr (kFp8) {
+#pragma unroll
+                for (int i = 0; i < kBN / 32; ++i) {
+                    const int col = n * kBN + 32 * i + lane;
+                    col_scale[i] = col < p.V ? __ldg(p.sw + col) : 0.0f;
+                }
+                row_scale = row < p.T ? __ldg(p.sh + row) : 0.0f;
+            }
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -311,8 +323,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float run_m = -INFINITY, run_s = 0.0f, zt = 0.0f;
                 int32_t run_a = INT_MAX;
                 float run_u = 0.0f;  // mode 2 only
-                float row_scale = 1.0f;
-                if constexpr (kFp8) row_scale = row < p.T ? __ldg(p.sh + row) : 0.0f;
                 const uint32_t t_addr = lane_base + acc * uint32_t(kBN);
                 for (int c = 0; c < nchunks; ++c) {
                     uint32_t r[32];
@@ -321,10 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float z[32];
                     const int nvalid = ncols - c * 32;
                     if constexpr (kFp8) {
-                        const float* swc = p.sw + col0 + c * 32;  // this launch's W rows
+                        float mine = col_scale[0];  // this chunk's scale held by this lane
+#pragma unroll
+                        for (int i = 1; i < kBN / 32; ++i)
+                            if (c == i) mine = col_scale[i];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const float cs_ = j < nvalid ? __ldg(swc + j) : 0.0f;
+                            const float cs_ = __shfl_sync(0xffffffffu, mine, j);
                             z[j] = __fmul_rn(__fmul_rn(__fmul_rn(__uint_as_float(r[j]), row_scale),
                                                        cs_),
                                              inv_temp);
