@@ -371,7 +371,9 @@ rlk_status rlk_quantize_fp8_rows(const void* x_bf16, int64_t rows, int64_t H, ui
 }
 
 namespace {
-int64_t fp8_h_rows(int64_t T) { return T < rlk::kMinTmaRows ? rlk::kMinTmaRows : T; }
+// The quantised h is padded with zero rows to whole 128-row tiles, so no TMA box
+// of it reaches past its end (zero codes either way: no result bit changes).
+int64_t fp8_h_rows(int64_t T) { return (T + kRowTile - 1) / kRowTile * kRowTile; }
 size_t round16(size_t b) { return (b + 15) / 16 * 16; }
 }  // namespace
 
