@@ -163,7 +163,8 @@ rlk_status prepare_maps(const void* h, const void* W, int64_t T, int64_t H, int6
         h = pad_buf;
         h_rows = rlk::kMinTmaRows;
     }
-    if (!encode_bf16_2d(th, h, h_rows, H, kRowTile) || !encode_bf16_2d(tw, W, V, H, kVocabTile))
+    if (!encode_bf16_2d(th, h, h_rows, H, kRowTile) ||
+        !encode_bf16_2d(tw, W, V, H, rlk::lmhead_w_box_rows(T)))
         return RLK_ERR_CUDA;
     return RLK_OK;
 }
@@ -429,10 +430,10 @@ rlk_status rlk_logprob_fp8(const void* hidden_bf16, const uint8_t* weight_e4m3,
     // the packed weight as rows of 128 bytes: blocks * kVocabTile of them
     const int64_t packed_rows = num_vocab_tiles(V) * (H / 128) * kVocabTile;
     if (!encode_2d(&th, qh, hrows, H, kRowTile, true) ||
-        !encode_2d(&tw, weight_e4m3, packed_rows, 128, kVocabTile, true))
+        !encode_2d(&tw, weight_e4m3, packed_rows, 128, rlk::lmhead_w_box_rows(T), true))
         return RLK_ERR_CUDA;
     e = rlk::launch_lmhead_partials_fp8(&th, &tw, targets_i32, sh, weight_scales_f32, workspace, T,
-                                        V, H, inv_temp, sms, s);
+                                        hrows, V, H, inv_temp, sms, s);
     if (e != cudaSuccess) return from_cuda(e);
     return from_cuda(rlk::launch_lse_merge(workspace, targets_i32, T, V, out_logp_f32, out_lse_f32,
                                            out_argmax_i32, s));

@@ -13,6 +13,14 @@ constexpr int kRowTile = 128;    // rows per tile  = UMMA M
 constexpr int kVocabTile = 256;  // columns per tile = UMMA N
 constexpr int kKBlock = 64;      // K elements per pipeline stage (one 128-B swizzle row)
 
+// The LM-head kernel runs as CTA pairs (tcgen05 cta_group::2, M = 256) when a
+// call has more than one row tile, and as single CTAs otherwise.  Either way a
+// row's logits come from the same K steps in the same order; the two variants
+// stage W in blocks of lmhead_w_box_rows(T) rows, which the W tensor map's box
+// height must equal.
+bool lmhead_use_pair(int64_t T);
+int lmhead_w_box_rows(int64_t T);
+
 // Calls with fewer rows than this get their h rows copied into a zero-padded
 // buffer of this many rows before the LM-head kernel runs (see rlk_pad.cu).
 constexpr int kMinTmaRows = 16;
@@ -22,7 +30,8 @@ cudaError_t launch_pad_rows(const void* h, int64_t T, int64_t H, void* dst, cuda
 
 // Fused LM-head GEMM + vocabulary-tile epilogue.  Writes partials[T][NVT]
 // (16-byte records {m, s, a, zt}).  th / tw are 2-D tensor maps of h [T,H] and
-// W [V,H] with boxes {kKBlock, kRowTile} / {kKBlock, kVocabTile}, 128-B swizzle.
+// W [V,H] with boxes {kKBlock, kRowTile} / {kKBlock, lmhead_w_box_rows(T)},
+// 128-B swizzle.
 // col_offset: global vocabulary index of tw's row 0 when tw maps a shard of W
 // (a multiple of kVocabTile); record indices `a` and target matching use global
 // columns, V is the number of rows tw maps.
@@ -54,14 +63,16 @@ cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, int
                                float* grad_W, bool accumulate_W, cudaStream_t stream);
 void release_backward_handles();
 
-// FP8 (e4m3) operands: th maps row-major uint8 codes with boxes {2*kKBlock, rows};
-// tw maps the tile-packed weight as [blocks * kVocabTile][128] with boxes
-// {128, kVocabTile} (box (n, kb) at row (n * num_kb + kb) * kVocabTile);
-// sh [rows of th] and sw [V] are the per-row scales; forward partials.
+// FP8 (e4m3) operands: th maps row-major uint8 codes [h_rows][H] with boxes
+// {2*kKBlock, kRowTile}; tw maps the tile-packed weight as
+// [blocks * kVocabTile][128] with boxes {128, lmhead_w_box_rows(T)} (block
+// (n, kb) at row (n * num_kb + kb) * kVocabTile); sh [h_rows] and sw [V] are
+// the per-row scales; forward partials.
 cudaError_t launch_lmhead_partials_fp8(const CUtensorMap* th, const CUtensorMap* tw,
                                        const int32_t* targets, const float* sh, const float* sw,
-                                       void* partials, int64_t T, int64_t V, int64_t H,
-                                       float inv_temp, int num_sms, cudaStream_t stream);
+                                       void* partials, int64_t T, int64_t h_rows, int64_t V,
+                                       int64_t H, float inv_temp, int num_sms,
+                                       cudaStream_t stream);
 
 // Per-row e4m3 quantisation of bf16 x [rows][H] into codes [out_rows][H] and
 // scales [out_rows]; rows >= `rows` are zero codes with scale 1.  H % 16 == 0.

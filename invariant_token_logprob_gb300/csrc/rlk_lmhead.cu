@@ -36,28 +36,44 @@
 #include "rlk_sm103.cuh"
 
 namespace rlk {
+
+bool lmhead_use_pair(int64_t T) { return T > kRowTile; }
+int lmhead_w_box_rows(int64_t T) { return lmhead_use_pair(T) ? kVocabTile / 2 : kVocabTile; }
+
 namespace {
 
 constexpr int kBM = kRowTile;
 constexpr int kBN = kVocabTile;
 constexpr int kBK = kKBlock;
 constexpr int kUK = 16;  // K per tcgen05.mma kind::f16
-constexpr int kStages = 4;
 constexpr int kAccBufs = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
-constexpr int kBBytes = kBN * kBK * 2;  // 32 KiB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
-constexpr int kBarriers = 2 * kStages + 2 * kAccBufs + 1;
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + size_t(kStages) * kStageBytes +
-                              kBarriers * 8 + 16;
-constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
+
+// Per-CTA pipeline shape.  Single CTA: the CTA stages a 128-row h block and the
+// whole 256-row W block of each k-block.  CTA pair: the even CTA's MMA (M = 256)
+// covers both CTAs' 128-row h blocks, and each CTA stages half (128 rows) of the
+// W block, so a stage is 32 KiB instead of 48 and six stages fit.
+template <bool kPair>
+struct Pipe {
+    static constexpr int kBRows = kPair ? kBN / 2 : kBN;  // W rows one CTA stages
+    static constexpr int kBBytes = kBRows * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = kPair ? 6 : 4;
+    static constexpr int kBarriers = 2 * kStages + 2 * kAccBufs + 1;
+    static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ +
+                                         size_t(kStages) * kStageBytes + kBarriers * 8 + 16;
+    static constexpr int kMmaM = kPair ? 2 * kBM : kBM;
+    static constexpr int kEpiArrivals = kPair ? 8 : 4;  // epilogue warps releasing a buffer
+    static_assert(kStageBytes % 1024 == 0, "stage tiles 1024-B aligned");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for teardown waits
 
 static_assert(kBK * 2 == 128, "one k-block is one 128-byte swizzle row");
-static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "stage tiles 1024-B aligned");
+static_assert(kABytes % 1024 == 0, "stage tiles 1024-B aligned");
 static_assert(kAccBufs * kBN <= int(kTmemCols), "TMEM budget");
 
 __device__ unsigned int g_lmhead_error;
@@ -70,12 +86,14 @@ struct Args {
     const float* grad;     // mode 1: upstream gradient of logp per row
     uint16_t* dz;          // mode 1: [T][V] bf16 gradient of logp w.r.t. the logits
     int64_t T;
+    int64_t h_rows; // rows the h tensor map covers (>= T; padded copies are longer)
     int V;          // columns of the W this launch sees (a shard's rows when sharded)
     int col_offset; // global vocabulary index of that W's row 0 (0 unless sharded)
     int num_m;   // row tiles
+    int num_mu;  // row units: row tiles (single CTA) or pairs of row tiles (CTA pair)
     int num_n;   // vocabulary tiles (NVT)
     int num_kb;  // k-blocks
-    int band;    // row tiles per raster band (schedule only; never affects values)
+    int band;    // row units per raster band (schedule only; never affects values)
     int num_tiles;
     float inv_temp;
     int stall_selftest;  // 1: the producer issues no copies (bounded-wait self-test)
@@ -83,28 +101,40 @@ struct Args {
     const float* sw;     // fp8 operands: per-row scale of W [V] (this launch's rows)
 };
 
-// Raster: bands of `band` row tiles; inside a band, vocabulary tile outer and
-// row tile inner, so CTAs running together share one W tile through L2 and
-// the band's h rows stay L2-resident while W streams past once per band.
-__device__ __forceinline__ void tile_coords(const Args& p, int tile, int& m, int& n) {
+// Raster over (row unit, vocabulary tile): bands of `band` row units; inside a
+// band, vocabulary tile outer and row unit inner, so the CTAs running together
+// share one W tile through L2 and the band's h rows stay L2-resident while W
+// streams past once per band.
+__device__ __forceinline__ void tile_coords(const Args& p, int tile, int& mu, int& n) {
     const int band_tiles = p.band * p.num_n;
     const int b = tile / band_tiles;
     const int rem = tile - b * band_tiles;
-    const int rows = min(p.band, p.num_m - b * p.band);
+    const int rows = min(p.band, p.num_mu - b * p.band);
     n = rem / rows;
-    m = b * p.band + (rem - n * rows);
+    mu = b * p.band + (rem - n * rows);
 }
 
 // Wait for phase `parity` of `bar`, giving up after kWaitLimitNs (then the
 // error word and the CTA's abort flag are set) or when another role of the
 // CTA has already given up.
+// kCluster: acquire at cluster scope (the barrier is arrived on by the other
+// CTA of a pair).
+template <bool kCluster = false>
+__device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
+    if constexpr (kCluster)
+        return mbar_try_wait_cluster(bar, parity);
+    else
+        return mbar_try_wait(bar, parity);
+}
+
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait_scoped<kCluster>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     uint32_t spins = 0;
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_wait_scoped<kCluster>(bar, parity)) return true;
         if ((++spins & 63u) == 0) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -141,13 +171,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // kFp8: e4m3 operands (tcgen05 kind::f8f6f4, K = 32 per MMA, 128 K-elements
 // per 128-byte stage row) with per-row scales of h and W applied to the fp32
 // accumulator in the epilogue: z = ((acc * s_h[row]) * s_W[col]) * inv_temp.
-template <int kMode, bool kFp8>
+//
+// kPair: launched in clusters of two CTAs on neighbouring SMs.  A work unit is
+// (pair of row tiles 2u, 2u+1; vocabulary tile n).  Both CTAs stage their own
+// 128 h rows and one half of the 256 W rows and signal the even CTA's stage
+// barrier; the even CTA's MMA warp issues tcgen05.mma.cta_group::2 (M = 256,
+// N = 256, K = 16 or 32), which leaves each CTA's 128 rows in its own TMEM,
+// and its commits release the stage and the accumulator in both CTAs.  Each
+// CTA's epilogue is the single-CTA epilogue over its own row tile and hands
+// the accumulator back on the even CTA's barrier.  A row still meets the same
+// K steps in the same order and the same epilogue; only the MMA instruction's
+// M (which rows it covers, never how one row is summed) and the copy routes
+// differ.
+template <int kMode, bool kFp8, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmap_h,
                   const __grid_constant__ CUtensorMap tmap_w, const Args p) {
     static_assert(!kFp8 || kMode == kModePartials, "fp8 operands: forward partials only");
+    using P = Pipe<kPair>;
+    constexpr int kG = kPair ? 2 : 1;  // tcgen05 CTA group
+    constexpr int kStages = P::kStages;
+    constexpr int kStageBytes = P::kStageBytes;
     constexpr int kBKE = kFp8 ? 2 * kBK : kBK;  // K elements per stage (128 bytes per row)
-    constexpr uint32_t kIdescT = kFp8 ? idesc_e4m3_f32(kBM, kBN) : kIdesc;
+    constexpr uint32_t kIdescT =
+        kFp8 ? idesc_e4m3_f32(P::kMmaM, kBN) : idesc_bf16_f32(P::kMmaM, kBN);
+    constexpr int kBarriers = P::kBarriers;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -175,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 4);  // one arrival per epilogue warp
+            mbar_init(tempty_bar(b), P::kEpiArrivals);  // one arrival per epilogue warp
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -186,13 +234,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmap_w);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<kG>(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish<kG>();
     }
     tc_fence_before_sync();
     __syncthreads();
+    // CTA pair: the other CTA's barriers must be initialised before anything
+    // arrives on them.
+    if constexpr (kPair) cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;        // CTA within the pair
+    const int slot = kPair ? int(cluster_id_x()) : int(blockIdx.x);  // work-unit stride
+    const int nslots = kPair ? int(num_clusters_x()) : int(gridDim.x);
     // Everything above touched only shared memory, TMEM and the kernel
     // parameters; the launch may overlap the previous kernel in the stream up to
     // here.  No global memory is read or written before this wait.
@@ -208,21 +262,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Self-test: no copy is ever issued, so the MMA warp's first wait can
             // only end by running out; everything else then sees the abort flag.
             const int ntiles = p.stall_selftest ? 0 : p.num_tiles;
-            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-                int m, n;
-                tile_coords(p, tile, m, n);
+            for (int tile = slot; ok && tile < ntiles; tile += nslots) {
+                int mu, n;
+                tile_coords(p, tile, mu, n);
+                // CTA pair: a block that lies wholly past the end of h (odd row
+                // tile of the last unit) or of W (odd half of the last vocabulary
+                // tile) is not copied; the MMA then reads stale shared memory for
+                // rows / columns that the epilogues never report.
+                uint32_t unit_bytes = kStageBytes;
+                bool load_a = true, load_b = true;
+                if constexpr (kPair) {
+                    unit_bytes = 0;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const bool la = int64_t(2 * mu + r) * kBM < p.h_rows;
+                        const bool lb = n * kBN + r * P::kBRows < p.V;
+                        unit_bytes += (la ? kABytes : 0) + (lb ? P::kBBytes : 0);
+                        if (uint32_t(r) == rank) {
+                            load_a = la;
+                            load_b = lb;
+                        }
+                    }
+                }
+                const int m = kPair ? 2 * mu + int(rank) : mu;     // this CTA's row tile
+                const int wrow = n * kBN + int(rank) * P::kBRows;  // its first W row
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-                    tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage), kb * kBKE, m * kBM);
-                    if constexpr (kFp8)  // tile-packed weight: one contiguous 32 KB block
-                        tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), 0,
-                                    (n * p.num_kb + kb) * kBN);
-                    else
-                        tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), kb * kBKE, n * kBN);
+                    if constexpr (kPair) {
+                        // both CTAs' copies complete on the even CTA's stage barrier
+                        const uint32_t fb = mapa_shared(full_bar(stage), 0);
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), unit_bytes);
+                        if (load_a)
+                            tma_load_2d_pair(&tmap_h, fb, a_tile(stage), kb * kBKE, m * kBM);
+                        if (load_b) {
+                            if constexpr (kFp8)  // tile-packed weight, 16 KB half block
+                                tma_load_2d_pair(&tmap_w, fb, b_tile(stage), 0,
+                                                 (n * p.num_kb + kb) * kBN +
+                                                     int(rank) * P::kBRows);
+                            else
+                                tma_load_2d_pair(&tmap_w, fb, b_tile(stage), kb * kBKE, wrow);
+                        }
+                    } else {
+                        mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+                        tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage), kb * kBKE, m * kBM);
+                        if constexpr (kFp8)  // tile-packed weight: one contiguous 32 KB block
+                            tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), 0,
+                                        (n * p.num_kb + kb) * kBN);
+                        else
+                            tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), kb * kBKE,
+                                        wrow);
+                    }
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -232,20 +324,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) {
                 // Let the copies this thread started land before the CTA exits.
-                const int first = issued > kStages ? issued - kStages : 0;
-                for (int i = first; i < issued; ++i)
-                    wait_drain(full_bar(i % kStages), uint32_t(i / kStages) & 1u);
+                if (!kPair || rank == 0) {
+                    const int first = issued > kStages ? issued - kStages : 0;
+                    for (int i = first; i < issued; ++i)
+                        wait_drain(full_bar(i % kStages), uint32_t(i / kStages) & 1u);
+                } else {
+                    // the odd CTA's copies signal the even CTA's barriers, which
+                    // it cannot wait on: give them a fixed time to land
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 1000000ull) {
+                    }
+                }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {  // CTA pair: the even CTA issues for both
             uint32_t stage = 0, phase = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
+            for (int tile = slot; ok && tile < p.num_tiles; tile += nslots) {
+                if (!wait_bounded<kPair>(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * uint32_t(kBN);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -262,27 +362,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // advance the start address by kk * 32 bytes inside the swizzle row
                         const uint64_t off = uint64_t((kk * 32) >> 4);
                         if constexpr (kFp8)
-                            umma_f8(d_tmem, a_desc + off, b_desc + off, kIdescT,
-                                    (kb | kk) != 0 ? 1u : 0u);
+                            umma_f8<kG>(d_tmem, a_desc + off, b_desc + off, kIdescT,
+                                        (kb | kk) != 0 ? 1u : 0u);
                         else
-                            umma_bf16(d_tmem, a_desc + off, b_desc + off, kIdescT,
-                                      (kb | kk) != 0 ? 1u : 0u);
+                            umma_bf16<kG>(d_tmem, a_desc + off, b_desc + off, kIdescT,
+                                          (kb | kk) != 0 ? 1u : 0u);
                     }
-                    umma_commit(empty_bar(stage));  // frees the smem stage when these MMAs finish
+                    // frees the smem stage (in both CTAs of a pair) when these MMAs finish
+                    if constexpr (kPair)
+                        umma_commit_pair_multicast(empty_bar(stage), 0x3);
+                    else
+                        umma_commit(empty_bar(stage));
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+                // accumulator ready for the epilogue(s)
+                if constexpr (kPair)
+                    umma_commit_pair_multicast(tfull_bar(acc), 0x3);
+                else
+                    umma_commit(tfull_bar(acc));
                 if (++acc == kAccBufs) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
             // No MMA may still be writing TMEM when it is freed.
-            umma_commit(drain_bar);
+            umma_commit<kG>(drain_bar);
             wait_drain(drain_bar, 0);
         }
         __syncwarp();
@@ -293,9 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16);
         const float inv_temp = p.inv_temp;
         uint32_t acc = 0, acc_phase = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-            int m, n;
-            tile_coords(p, tile, m, n);
+        for (int tile = slot; tile < p.num_tiles; tile += nslots) {
+            int mu, n;
+            tile_coords(p, tile, mu, n);
+            const int m = kPair ? 2 * mu + int(rank) : mu;
             const int64_t row = int64_t(m) * kBM + row_in_tile;
             const int32_t tgt = row < p.T ? __ldg(p.targets + row) : -1;
             // fp8: fetch the tile's 256 column scales now, while the MMAs run --
@@ -382,7 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Accumulator buffer fully read: hand it back to the MMA warp.
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                if (lane == 0) {
+                    if constexpr (kPair)  // the even CTA's accumulator-empty barrier
+                        mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+                    else
+                        mbar_arrive(tempty_bar(acc));
+                }
                 if (row < p.T) {
                     p.partials[row * p.num_n + n] =
                         make_float4(run_m, run_s, __int_as_float(run_a), zt);
@@ -435,7 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                if (lane == 0) {
+                    if constexpr (kPair)  // the even CTA's accumulator-empty barrier
+                        mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+                    else
+                        mbar_arrive(tempty_bar(acc));
+                }
             }
             if (++acc == kAccBufs) {
                 acc = 0;
@@ -446,47 +565,92 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    // CTA pair: neither CTA frees its TMEM or leaves while the pair's MMAs or
+    // the other CTA's arrivals may still reach it.
+    if constexpr (kPair) cluster_sync();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc<kG>(tmem_base, kTmemCols);
     }
+    if constexpr (kPair) cluster_sync();
 }
 
-int g_configured[4][64];  // per kernel variant and device: smem attribute set
+struct VariantState {
+    int configured = 0;    // dynamic shared memory attribute set
+    int max_clusters = 0;  // CTA pairs that fit at once (CTA-pair variants)
+};
+VariantState g_variant[8][64];  // per kernel variant and device
 
-template <int kMode, bool kFp8 = false>
-cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, int64_t H,
-                        int num_sms, cudaStream_t stream) {
-    constexpr int kVariant = kFp8 ? 3 : kMode;
+template <int kMode, bool kFp8, bool kPair>
+cudaError_t launch_variant(const CUtensorMap* th, const CUtensorMap* tw, Args a, int64_t H,
+                           int num_sms, cudaStream_t stream) {
+    using P = Pipe<kPair>;
+    constexpr int kVariant = (kFp8 ? 3 : kMode) + (kPair ? 4 : 0);
     constexpr int kBKE = kFp8 ? 2 * kBK : kBK;
+    auto kernel = lmhead_kernel<kMode, kFp8, kPair>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && !g_configured[kVariant][dev]) {
-        e = cudaFuncSetAttribute(lmhead_kernel<kMode, kFp8>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
-        if (e != cudaSuccess) return e;
-        g_configured[kVariant][dev] = 1;
-    }
-    a.num_m = int((a.T + kBM - 1) / kBM);
-    a.num_n = int((a.V + kBN - 1) / kBN);
-    a.num_kb = int((H + kBKE - 1) / kBKE);
-    a.band = a.num_m < 32 ? a.num_m : 32;
-    a.num_tiles = a.num_m * a.num_n;
-    const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    VariantState& vs = g_variant[kVariant][dev];
+
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(grid, 1, 1);
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = kPair ? 2 : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = P::kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, lmhead_kernel<kMode, kFp8>, *th, *tw, a);
+    cfg.numAttrs = kPair ? 2 : 1;
+
+    if (!vs.configured) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(P::kSmemBytes));
+        if (e != cudaSuccess) return e;
+        if constexpr (kPair) {
+            // how many CTA pairs the GPU holds at once (pairs need two SMs of
+            // one GPC); the persistent grid is sized to it
+            cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+            if (e != cudaSuccess || n < 1) {
+                cudaGetLastError();
+                n = num_sms / 2;
+            }
+            vs.max_clusters = n;
+        }
+        vs.configured = 1;
+    }
+    a.num_m = int((a.T + kBM - 1) / kBM);
+    a.num_mu = kPair ? (a.num_m + 1) / 2 : a.num_m;
+    a.num_n = int((a.V + kBN - 1) / kBN);
+    a.num_kb = int((H + kBKE - 1) / kBKE);
+    a.band = kPair ? (a.num_mu < 16 ? a.num_mu : 16) : (a.num_mu < 32 ? a.num_mu : 32);
+    a.num_tiles = a.num_mu * a.num_n;
+    if constexpr (kPair) {
+        const int clusters = a.num_tiles < vs.max_clusters ? a.num_tiles : vs.max_clusters;
+        cfg.gridDim = dim3(2 * clusters, 1, 1);
+    } else {
+        cfg.gridDim = dim3(a.num_tiles < num_sms ? a.num_tiles : num_sms, 1, 1);
+    }
+    e = cudaLaunchKernelEx(&cfg, kernel, *th, *tw, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// Calls with more than one row tile run the CTA-pair variant.
+template <int kMode, bool kFp8 = false>
+cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, int64_t H,
+                        int num_sms, cudaStream_t stream) {
+    if (a.h_rows == 0) a.h_rows = a.T;
+    if (lmhead_use_pair(a.T) && !a.stall_selftest)
+        return launch_variant<kMode, kFp8, true>(th, tw, a, H, num_sms, stream);
+    return launch_variant<kMode, kFp8, false>(th, tw, a, H, num_sms, stream);
 }
 
 }  // namespace
@@ -521,14 +685,16 @@ cudaError_t launch_lmhead_entropy(const CUtensorMap* th, const CUtensorMap* tw,
 
 cudaError_t launch_lmhead_partials_fp8(const CUtensorMap* th, const CUtensorMap* tw,
                                        const int32_t* targets, const float* sh, const float* sw,
-                                       void* partials, int64_t T, int64_t V, int64_t H,
-                                       float inv_temp, int num_sms, cudaStream_t stream) {
+                                       void* partials, int64_t T, int64_t h_rows, int64_t V,
+                                       int64_t H, float inv_temp, int num_sms,
+                                       cudaStream_t stream) {
     Args a = {};
     a.targets = targets;
     a.partials = static_cast<float4*>(partials);
     a.sh = sh;
     a.sw = sw;
     a.T = T;
+    a.h_rows = h_rows;
     a.V = int(V);
     a.inv_temp = inv_temp;
     return launch_mode<kModePartials, true>(th, tw, a, H, num_sms, stream);
