@@ -308,6 +308,23 @@ rlk_status rlk_consistency_stats(const float *logp_a, const float *logp_b,
                                  rlk_stream_t stream);
 
 /*
+ * The same statistics, stream-ordered and without allocation: for training
+ * loops that log them per step and must not stall the GPU on a host read-back.
+ *   out_device  device, 8 doubles (8-byte aligned): the layout of `out` above,
+ *               written when the launched kernels complete (n == 0 included)
+ *   workspace   device, >= rlk_consistency_stats_workspace_size(n) bytes,
+ *               16-byte aligned, caller-owned (may be reused once the call's
+ *               kernels have completed in stream order)
+ * Asynchronous on `stream`.  Bit-identical to rlk_consistency_stats for the
+ * same inputs (same kernels, same fixed reduction order).
+ */
+size_t rlk_consistency_stats_workspace_size(int64_t n);
+rlk_status rlk_consistency_stats_async(const float *logp_a, const float *logp_b,
+                                       const int8_t *mask, int64_t n, double *out_device,
+                                       void *workspace, size_t workspace_bytes,
+                                       rlk_stream_t stream);
+
+/*
  * rlk_logprob for callers that cannot allocate device memory.  The pages
  * describe no counterpart of this entry point; it exists for this library's
  * users.  Callers that cannot allocate include code running under CUDA-graph

@@ -77,6 +77,10 @@ def lib() -> ctypes.CDLL:
         L.rlk_lse_merge.argtypes = [P, P, i64, i64, P, P, P, P]
         L.rlk_consistency_stats.restype = st
         L.rlk_consistency_stats.argtypes = [P, P, P, i64, P, P]
+        L.rlk_consistency_stats_workspace_size.restype = sz
+        L.rlk_consistency_stats_workspace_size.argtypes = [i64]
+        L.rlk_consistency_stats_async.restype = st
+        L.rlk_consistency_stats_async.argtypes = [P, P, P, i64, P, P, sz, P]
         L.rlk_selftest_wait_timeout.restype = st
         L.rlk_selftest_wait_timeout.argtypes = [P, P, P, P, P]
         L.rlk_check_device_error.restype = st
@@ -253,6 +257,46 @@ def consistency_stats(a, b, mask=None, stream=None):
     _check(lib().rlk_consistency_stats(_ptr(a), _ptr(b), mp, a.shape[0], out, _stream(stream)),
            "rlk_consistency_stats")
     return dict(zip(STAT_NAMES, list(out)))
+
+
+def consistency_stats_async(a, b, mask=None, out=None, workspace=None, stream=None):
+    """rlk_consistency_stats_async: the same statistics written, stream-ordered, into a
+    float64 CUDA tensor of 8 (returned; pass `out` to reuse one).  No host sync and no
+    allocation inside the library; read it with stats_dict() when needed."""
+    import torch
+    _need(a, torch.float32, "a", 1)
+    _need(b, torch.float32, "b", 1)
+    if a.shape != b.shape:
+        raise ValueError("a and b must have the same shape")
+    mp = None
+    if mask is not None:
+        _need(mask, torch.int8, "mask", 1)
+        if mask.shape != a.shape:
+            raise ValueError("mask must match a")
+        mp = _ptr(mask)
+    n = a.shape[0]
+    if out is None:
+        out = torch.empty(8, dtype=torch.float64, device=a.device)
+    _need(out, torch.float64, "out", 1)
+    if out.numel() < 8:
+        raise ValueError("out must hold 8 doubles")
+    need = lib().rlk_consistency_stats_workspace_size(n)
+    if workspace is None:
+        workspace = torch.empty(max(16, need), dtype=torch.uint8, device=a.device)
+    _need(workspace, torch.uint8, "workspace", 1)
+    _check(lib().rlk_consistency_stats_async(_ptr(a), _ptr(b), mp, n, _ptr(out), _ptr(workspace),
+                                             workspace.numel(), _stream(stream)),
+           "rlk_consistency_stats_async")
+    return out
+
+
+def stats_workspace_size(n: int) -> int:
+    return lib().rlk_consistency_stats_workspace_size(int(n))
+
+
+def stats_dict(out):
+    """The 8 statistics of a consistency_stats_async result as a dict (synchronises)."""
+    return dict(zip(STAT_NAMES, out.cpu().tolist()))
 
 
 def check_device_error(stream=None):

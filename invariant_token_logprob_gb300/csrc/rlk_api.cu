@@ -536,6 +536,31 @@ rlk_status rlk_consistency_stats(const float* logp_a, const float* logp_b, const
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t rlk_consistency_stats_workspace_size(int64_t n) {
+    if (n < 0) return 0;
+    return rlk::consistency_stats_workspace_bytes(n);
+}
+
+rlk_status rlk_consistency_stats_async(const float* logp_a, const float* logp_b,
+                                       const int8_t* mask, int64_t n, double* out_device,
+                                       void* workspace, size_t workspace_bytes,
+                                       rlk_stream_t stream) {
+    if (!out_device || n < 0) return RLK_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out_device) & 7u) != 0) return RLK_ERR_ALIGNMENT;
+    if (n > 0) {
+        if (!logp_a || !logp_b) return RLK_ERR_INVALID_ARG;
+        if (!aligned4(logp_a) || !aligned4(logp_b)) return RLK_ERR_ALIGNMENT;
+        if (!workspace) return RLK_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return RLK_ERR_ALIGNMENT;
+        if (workspace_bytes < rlk::consistency_stats_workspace_bytes(n)) return RLK_ERR_WORKSPACE;
+    }
+    int dev, sms;
+    rlk_status st = current_device(&dev, &sms);
+    if (st != RLK_OK) return st;
+    return from_cuda(rlk::launch_consistency_stats(logp_a, logp_b, mask, n, out_device, workspace,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 rlk_status rlk_selftest_wait_timeout(const void* hidden_bf16, const void* weight_bf16,
                                      const int32_t* targets_i32, rlk_partial* partials,
                                      rlk_stream_t stream) {

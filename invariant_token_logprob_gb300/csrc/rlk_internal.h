@@ -118,4 +118,11 @@ cudaError_t launch_lse_merge(const void* partials, const int32_t* targets, int64
 cudaError_t run_consistency_stats(const float* a, const float* b, const int8_t* mask, int64_t n,
                                   double* host_out, cudaStream_t stream);
 
+// The same, stream-ordered: result in device memory (8 doubles); workspace of
+// consistency_stats_workspace_bytes(n) bytes.
+size_t consistency_stats_workspace_bytes(int64_t n);
+cudaError_t launch_consistency_stats(const float* a, const float* b, const int8_t* mask,
+                                     int64_t n, double* device_out, void* workspace,
+                                     cudaStream_t stream);
+
 }  // namespace rlk

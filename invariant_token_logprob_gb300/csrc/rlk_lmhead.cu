@@ -59,8 +59,10 @@ template <bool kPair>
 struct Pipe {
     static constexpr int kBRows = kPair ? kBN / 2 : kBN;  // W rows one CTA stages
     static constexpr int kBBytes = kBRows * kBK * 2;
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = kPair ? 6 : 4;
+    static constexpr int kKbBytes = kABytes + kBBytes;    // one k-block: h block + W block
+    static constexpr int kKbPerStage = kPair ? 2 : 1;     // k-blocks per stage (one barrier)
+    static constexpr int kStageBytes = kKbPerStage * kKbBytes;
+    static constexpr int kStages = kPair ? 3 : 4;
     static constexpr int kBarriers = 2 * kStages + 2 * kAccBufs + 1;
     static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ +
                                          size_t(kStages) * kStageBytes + kBarriers * 8 + 16;
@@ -210,8 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * kStages + b); };
     auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * kStages + kAccBufs + b); };
     const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 2 * kAccBufs);
-    auto a_tile = [&](int s) { return tiles_addr + uint32_t(s) * kStageBytes; };
-    auto b_tile = [&](int s) { return tiles_addr + uint32_t(s) * kStageBytes + kABytes; };
+    // k-block j of stage s: h block, then W block
+    auto a_tile = [&](int s, int j) {
+        return tiles_addr + uint32_t(s) * kStageBytes + uint32_t(j) * P::kKbBytes;
+    };
+    auto b_tile = [&](int s, int j) { return a_tile(s, j) + kABytes; };
+    constexpr int kKbs = P::kKbPerStage;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -269,15 +275,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tile of the last unit) or of W (odd half of the last vocabulary
                 // tile) is not copied; the MMA then reads stale shared memory for
                 // rows / columns that the epilogues never report.
-                uint32_t unit_bytes = kStageBytes;
+                uint32_t kb_bytes = P::kKbBytes;  // per k-block, both CTAs of a pair
                 bool load_a = true, load_b = true;
                 if constexpr (kPair) {
-                    unit_bytes = 0;
+                    kb_bytes = 0;
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         const bool la = int64_t(2 * mu + r) * kBM < p.h_rows;
                         const bool lb = n * kBN + r * P::kBRows < p.V;
-                        unit_bytes += (la ? kABytes : 0) + (lb ? P::kBBytes : 0);
+                        kb_bytes += (la ? kABytes : 0) + (lb ? P::kBBytes : 0);
                         if (uint32_t(r) == rank) {
                             load_a = la;
                             load_b = lb;
@@ -286,34 +292,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int m = kPair ? 2 * mu + int(rank) : mu;     // this CTA's row tile
                 const int wrow = n * kBN + int(rank) * P::kBRows;  // its first W row
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb0 = 0; kb0 < p.num_kb; kb0 += kKbs) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
+                    const int nkb = min(kKbs, p.num_kb - kb0);  // k-blocks in this stage
                     if constexpr (kPair) {
                         // both CTAs' copies complete on the even CTA's stage barrier
                         const uint32_t fb = mapa_shared(full_bar(stage), 0);
-                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), unit_bytes);
-                        if (load_a)
-                            tma_load_2d_pair(&tmap_h, fb, a_tile(stage), kb * kBKE, m * kBM);
-                        if (load_b) {
-                            if constexpr (kFp8)  // tile-packed weight, 16 KB half block
-                                tma_load_2d_pair(&tmap_w, fb, b_tile(stage), 0,
-                                                 (n * p.num_kb + kb) * kBN +
-                                                     int(rank) * P::kBRows);
-                            else
-                                tma_load_2d_pair(&tmap_w, fb, b_tile(stage), kb * kBKE, wrow);
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), nkb * kb_bytes);
+                        for (int j = 0; j < nkb; ++j) {
+                            const int kb = kb0 + j;
+                            if (load_a)
+                                tma_load_2d_pair(&tmap_h, fb, a_tile(stage, j), kb * kBKE,
+                                                 m * kBM);
+                            if (load_b) {
+                                if constexpr (kFp8)  // tile-packed weight, 16 KB half block
+                                    tma_load_2d_pair(&tmap_w, fb, b_tile(stage, j), 0,
+                                                     (n * p.num_kb + kb) * kBN +
+                                                         int(rank) * P::kBRows);
+                                else
+                                    tma_load_2d_pair(&tmap_w, fb, b_tile(stage, j), kb * kBKE,
+                                                     wrow);
+                            }
                         }
                     } else {
-                        mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-                        tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage), kb * kBKE, m * kBM);
-                        if constexpr (kFp8)  // tile-packed weight: one contiguous 32 KB block
-                            tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), 0,
-                                        (n * p.num_kb + kb) * kBN);
-                        else
-                            tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), kb * kBKE,
-                                        wrow);
+                        mbar_arrive_expect_tx(full_bar(stage), nkb * kb_bytes);
+                        for (int j = 0; j < nkb; ++j) {
+                            const int kb = kb0 + j;
+                            tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage, j), kb * kBKE,
+                                        m * kBM);
+                            if constexpr (kFp8)  // tile-packed weight: one contiguous 32 KB block
+                                tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage, j), 0,
+                                            (n * p.num_kb + kb) * kBN);
+                            else
+                                tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage, j),
+                                            kb * kBKE, wrow);
+                        }
                     }
                     ++issued;
                     if (++stage == kStages) {
@@ -348,25 +364,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bounded<kPair>(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * uint32_t(kBN);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb0 = 0; kb0 < p.num_kb; kb0 += kKbs) {
                     if (!wait_bounded(full_bar(stage), phase, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage));
-                    const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage));
+                    const int nkb = min(kKbs, p.num_kb - kb0);
+                    for (int j = 0; j < nkb; ++j) {
+                        const int kb = kb0 + j;
+                        const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage, j));
+                        const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage, j));
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        // each MMA consumes 32 bytes of every row (16 bf16 or 32 e4m3):
-                        // advance the start address by kk * 32 bytes inside the swizzle row
-                        const uint64_t off = uint64_t((kk * 32) >> 4);
-                        if constexpr (kFp8)
-                            umma_f8<kG>(d_tmem, a_desc + off, b_desc + off, kIdescT,
-                                        (kb | kk) != 0 ? 1u : 0u);
-                        else
-                            umma_bf16<kG>(d_tmem, a_desc + off, b_desc + off, kIdescT,
-                                          (kb | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            // each MMA consumes 32 bytes of every row (16 bf16 or 32 e4m3):
+                            // advance the start address by kk * 32 bytes in the swizzle row
+                            const uint64_t off = uint64_t((kk * 32) >> 4);
+                            if constexpr (kFp8)
+                                umma_f8<kG>(d_tmem, a_desc + off, b_desc + off, kIdescT,
+                                            (kb | kk) != 0 ? 1u : 0u);
+                            else
+                                umma_bf16<kG>(d_tmem, a_desc + off, b_desc + off, kIdescT,
+                                              (kb | kk) != 0 ? 1u : 0u);
+                        }
                     }
                     // frees the smem stage (in both CTAs of a pair) when these MMAs finish
                     if constexpr (kPair)

@@ -4,12 +4,15 @@
 // |p_rollout - p_train| and the k3 KL estimator r - 1 - log r).
 //
 // d = a - b in double (a = train, b = rollout), r = exp(d), k3 = expm1(d) - d.
-// Pass 1: block b owns the fixed slice [b*kChunk, (b+1)*kChunk); each thread
-// walks it with stride 256, then a fixed shared-memory tree reduces the block
-// (count, sum|d|, sum d, sum k3, max|d|, bit mismatches, first mismatch), and a
-// second walk over the same slice gives the block's sum (|d| - mean_b)^2.
-// Pass 2: one thread folds the blocks in index order (Chan's pairwise update
-// for the squared deviations).  Same n -> same order -> same bits.
+// Every valid position is a summary {count 1, |d|, d, k3, max |d|, bit
+// mismatch, first mismatch index, squared deviation 0}; summaries combine with
+// Chan's pairwise update for the squared deviations about the mean of |d|.
+// Pass 1: block b owns the fixed slice [256 b, 256 b + 256), one position per
+// thread, and combines them in a fixed tree (warp shuffles, then the 8 warps).
+// Pass 2: one block folds block summary j into thread j % 256 in index order,
+// then the same fixed tree.  Same n -> same tree -> same bits.  Slices are
+// small because the double-precision work (expm1 per position) is slow on
+// this GPU: it must be spread over many SMs.
 #include <math.h>
 
 #include "rlk_internal.h"
@@ -18,11 +21,72 @@ namespace rlk {
 namespace {
 
 constexpr int kStatThreads = 256;
-constexpr int64_t kChunk = 16384;
+constexpr int64_t kChunk = kStatThreads;  // positions per block
 
 struct Part {
     double n, sabs, sd, sk3, mx, nmis, first, m2;
 };
+
+__device__ __forceinline__ Part empty_part() {
+    Part r;
+    r.n = r.sabs = r.sd = r.sk3 = r.mx = r.nmis = r.m2 = 0.0;
+    r.first = -1.0;
+    return r;
+}
+
+// Combination of two summaries.  Commutative bit for bit (every operation is
+// symmetric in x and y), so shuffle trees need no care about operand order.
+__device__ __forceinline__ Part combine(const Part& x, const Part& y) {
+    Part r;
+    r.n = x.n + y.n;
+    r.m2 = x.m2 + y.m2;
+    if (x.n > 0 && y.n > 0) {
+        const double delta = y.sabs / y.n - x.sabs / x.n;
+        r.m2 += delta * delta * (x.n * y.n / r.n);
+    }
+    r.sabs = x.sabs + y.sabs;
+    r.sd = x.sd + y.sd;
+    r.sk3 = x.sk3 + y.sk3;
+    r.mx = x.mx > y.mx ? x.mx : y.mx;
+    r.nmis = x.nmis + y.nmis;
+    r.first = x.first < 0 ? y.first : (y.first < 0 ? x.first : (x.first < y.first ? x.first : y.first));
+    return r;
+}
+
+__device__ __forceinline__ Part shfl_down_part(const Part& v, int off) {
+    Part r;
+    r.n = __shfl_down_sync(0xffffffffu, v.n, off);
+    r.sabs = __shfl_down_sync(0xffffffffu, v.sabs, off);
+    r.sd = __shfl_down_sync(0xffffffffu, v.sd, off);
+    r.sk3 = __shfl_down_sync(0xffffffffu, v.sk3, off);
+    r.mx = __shfl_down_sync(0xffffffffu, v.mx, off);
+    r.nmis = __shfl_down_sync(0xffffffffu, v.nmis, off);
+    r.first = __shfl_down_sync(0xffffffffu, v.first, off);
+    r.m2 = __shfl_down_sync(0xffffffffu, v.m2, off);
+    return r;
+}
+
+// Fixed tree over the 256 threads' summaries; the result is valid in thread 0.
+__device__ Part block_combine(Part v) {
+    __shared__ Part warp_part[kStatThreads / 32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const Part o = shfl_down_part(v, off);
+        if (lane < off) v = combine(v, o);
+    }
+    if (lane == 0) warp_part[wid] = v;
+    __syncthreads();
+    if (wid == 0) {
+        v = lane < kStatThreads / 32 ? warp_part[lane] : empty_part();
+#pragma unroll
+        for (int off = 4; off >= 1; off >>= 1) {
+            const Part o = shfl_down_part(v, off);
+            if (lane < off) v = combine(v, o);
+        }
+    }
+    return v;
+}
 
 __device__ __forceinline__ bool valid_at(const int8_t* mask, int64_t i) {
     return mask == nullptr || mask[i] != 0;
@@ -31,126 +95,75 @@ __device__ __forceinline__ bool valid_at(const int8_t* mask, int64_t i) {
 __global__ void __launch_bounds__(kStatThreads)
     stats_block_kernel(const float* __restrict__ a, const float* __restrict__ b,
                        const int8_t* __restrict__ mask, int64_t n, Part* __restrict__ parts) {
-    __shared__ double sh[7][kStatThreads];
-    __shared__ double red[kStatThreads];
-    __shared__ double mean_sh;
-    const int tid = threadIdx.x;
-    const int64_t lo = int64_t(blockIdx.x) * kChunk;
-    const int64_t hi = lo + kChunk < n ? lo + kChunk : n;
-
-    double cnt = 0, sabs = 0, sd = 0, sk3 = 0, mx = 0, nmis = 0, first = -1;
-    for (int64_t i = lo + tid; i < hi; i += kStatThreads) {
-        if (!valid_at(mask, i)) continue;
+    const int64_t i = int64_t(blockIdx.x) * kChunk + threadIdx.x;
+    Part v = empty_part();
+    if (i < n && valid_at(mask, i)) {
         const float fa = a[i], fb = b[i];
         const double d = double(fa) - double(fb);
         const double ad = fabs(d);
-        cnt += 1;
-        sabs += ad;
-        sd += d;
-        sk3 += expm1(d) - d;
-        mx = ad > mx ? ad : mx;
+        v.n = 1.0;
+        v.sabs = ad;
+        v.sd = d;
+        v.sk3 = expm1(d) - d;
+        v.mx = ad;
         if (__float_as_uint(fa) != __float_as_uint(fb)) {
-            nmis += 1;
-            if (first < 0) first = double(i);
+            v.nmis = 1.0;
+            v.first = double(i);
         }
     }
-    sh[0][tid] = cnt;
-    sh[1][tid] = sabs;
-    sh[2][tid] = sd;
-    sh[3][tid] = sk3;
-    sh[4][tid] = mx;
-    sh[5][tid] = nmis;
-    sh[6][tid] = first;
-    __syncthreads();
-    for (int w = kStatThreads / 2; w > 0; w >>= 1) {
-        if (tid < w) {
-            sh[0][tid] += sh[0][tid + w];
-            sh[1][tid] += sh[1][tid + w];
-            sh[2][tid] += sh[2][tid + w];
-            sh[3][tid] += sh[3][tid + w];
-            sh[4][tid] = sh[4][tid] > sh[4][tid + w] ? sh[4][tid] : sh[4][tid + w];
-            sh[5][tid] += sh[5][tid + w];
-            const double f0 = sh[6][tid], f1 = sh[6][tid + w];
-            sh[6][tid] = f0 < 0 ? f1 : (f1 < 0 ? f0 : (f0 < f1 ? f0 : f1));
-        }
-        __syncthreads();
-    }
-    if (tid == 0) mean_sh = sh[0][0] > 0 ? sh[1][0] / sh[0][0] : 0.0;
-    __syncthreads();
-    const double mean = mean_sh;
-    double m2 = 0;
-    for (int64_t i = lo + tid; i < hi; i += kStatThreads) {
-        if (!valid_at(mask, i)) continue;
-        const double ad = fabs(double(a[i]) - double(b[i]));
-        m2 += (ad - mean) * (ad - mean);
-    }
-    red[tid] = m2;
-    __syncthreads();
-    for (int w = kStatThreads / 2; w > 0; w >>= 1) {
-        if (tid < w) red[tid] += red[tid + w];
-        __syncthreads();
-    }
-    if (tid == 0) {
-        Part pr;
-        pr.n = sh[0][0];
-        pr.sabs = sh[1][0];
-        pr.sd = sh[2][0];
-        pr.sk3 = sh[3][0];
-        pr.mx = sh[4][0];
-        pr.nmis = sh[5][0];
-        pr.first = sh[6][0];
-        pr.m2 = red[0];
-        parts[blockIdx.x] = pr;
-    }
+    v = block_combine(v);
+    if (threadIdx.x == 0) parts[blockIdx.x] = v;
 }
 
-__global__ void stats_final_kernel(const Part* __restrict__ parts, int64_t nblk,
-                                   double* __restrict__ out) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    double n = 0, sabs = 0, sd = 0, sk3 = 0, mx = 0, nmis = 0, first = -1, m2 = 0;
-    for (int64_t j = 0; j < nblk; ++j) {
-        const Part q = parts[j];
-        if (q.n > 0) {
-            const double ma = n > 0 ? sabs / n : 0.0;
-            const double mb = q.sabs / q.n;
-            const double delta = mb - ma;
-            m2 = m2 + q.m2 + delta * delta * (n * q.n / (n + q.n));
-        }
-        n += q.n;
-        sabs += q.sabs;
-        sd += q.sd;
-        sk3 += q.sk3;
-        mx = q.mx > mx ? q.mx : mx;
-        nmis += q.nmis;
-        if (first < 0 && q.first >= 0) first = q.first;
+__global__ void __launch_bounds__(kStatThreads)
+    stats_final_kernel(const Part* __restrict__ parts, int64_t nblk, double* __restrict__ out) {
+    Part v = empty_part();
+    for (int64_t j = threadIdx.x; j < nblk; j += kStatThreads) v = combine(v, parts[j]);
+    v = block_combine(v);
+    if (threadIdx.x == 0) {
+        out[0] = v.mx;
+        out[1] = v.n > 0 ? v.sabs / v.n : 0.0;
+        out[2] = v.n > 0 ? sqrt(v.m2 / v.n) : 0.0;
+        out[3] = v.n > 0 ? v.sk3 / v.n : 0.0;
+        out[4] = v.sd;
+        out[5] = v.n;
+        out[6] = v.nmis;
+        out[7] = v.first;
     }
-    out[0] = mx;
-    out[1] = n > 0 ? sabs / n : 0.0;
-    out[2] = n > 0 ? sqrt(m2 / n) : 0.0;
-    out[3] = n > 0 ? sk3 / n : 0.0;
-    out[4] = sd;
-    out[5] = n;
-    out[6] = nmis;
-    out[7] = first;
 }
 
 }  // namespace
 
+size_t consistency_stats_workspace_bytes(int64_t n) {
+    const int64_t nblk = n > 0 ? (n + kChunk - 1) / kChunk : 0;
+    return size_t(nblk) * sizeof(Part);
+}
+
+// Block partials into `workspace`, then the ordered fold into device_out.
+// n == 0: no block kernel; the fold of zero blocks writes the empty result.
+cudaError_t launch_consistency_stats(const float* a, const float* b, const int8_t* mask,
+                                     int64_t n, double* device_out, void* workspace,
+                                     cudaStream_t stream) {
+    const int64_t nblk = n > 0 ? (n + kChunk - 1) / kChunk : 0;
+    Part* parts = static_cast<Part*>(workspace);
+    if (nblk > 0) {
+        stats_block_kernel<<<unsigned(nblk), kStatThreads, 0, stream>>>(a, b, mask, n, parts);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    stats_final_kernel<<<1, kStatThreads, 0, stream>>>(parts, nblk, device_out);
+    return cudaGetLastError();
+}
+
 cudaError_t run_consistency_stats(const float* a, const float* b, const int8_t* mask, int64_t n,
                                   double* host_out, cudaStream_t stream) {
-    const int64_t nblk = (n + kChunk - 1) / kChunk;
     void* buf = nullptr;
-    const size_t bytes = size_t(nblk) * sizeof(Part) + 8 * sizeof(double);
+    const size_t part_bytes = (consistency_stats_workspace_bytes(n) + 15) / 16 * 16;
+    const size_t bytes = part_bytes + 8 * sizeof(double);
     cudaError_t e = cudaMallocAsync(&buf, bytes, stream);
     if (e != cudaSuccess) return e;
-    Part* parts = static_cast<Part*>(buf);
-    double* dout = reinterpret_cast<double*>(parts + nblk);
-    stats_block_kernel<<<unsigned(nblk), kStatThreads, 0, stream>>>(a, b, mask, n, parts);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) {
-        stats_final_kernel<<<1, 32, 0, stream>>>(parts, nblk, dout);
-        e = cudaGetLastError();
-    }
+    double* dout = reinterpret_cast<double*>(static_cast<char*>(buf) + part_bytes);
+    e = launch_consistency_stats(a, b, mask, n, dout, buf, stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync(host_out, dout, 8 * sizeof(double),
                                               cudaMemcpyDeviceToHost, stream);
     cudaError_t e2 = cudaFreeAsync(buf, stream);

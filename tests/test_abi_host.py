@@ -91,6 +91,28 @@ def test_stats_host_paths(L):
     assert list(out) == [0.0] * 7 + [-1.0]
 
 
+def test_stats_async_host_checks(L):
+    L.rlk_consistency_stats_workspace_size.restype = ctypes.c_size_t
+    L.rlk_consistency_stats_workspace_size.argtypes = [ctypes.c_int64]
+    f = L.rlk_consistency_stats_async
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_size_t, ctypes.c_void_p]
+    # one 64-byte block record per 256 elements, none for n <= 0
+    assert L.rlk_consistency_stats_workspace_size(0) == 0
+    assert L.rlk_consistency_stats_workspace_size(-3) == 0
+    assert L.rlk_consistency_stats_workspace_size(1) == 64
+    assert L.rlk_consistency_stats_workspace_size(256) == 64
+    assert L.rlk_consistency_stats_workspace_size(257) == 128
+    assert f(A16, A16, None, -1, A16, A16, 1 << 20, None) == 1          # n < 0
+    assert f(A16, A16, None, 5, None, A16, 1 << 20, None) == 1          # no output
+    assert f(A16, A16, None, 5, A4, A16, 1 << 20, None) == 2            # output not 8-aligned
+    assert f(None, A16, None, 5, A16, A16, 1 << 20, None) == 1          # no input
+    assert f(A16, A16, None, 5, A16, None, 1 << 20, None) == 5          # no workspace
+    assert f(A16, A16, None, 5, A16, A16, 8, None) == 5                 # workspace too small
+    assert f(A16, A16, None, 5, A16, A4, 1 << 20, None) == 2            # workspace misaligned
+
+
 def test_valid_call_without_gpu_reports_device_error(L):
     """On a machine without a GB300 a well-formed call fails with a status,
     never silently computes on the CPU."""

@@ -175,6 +175,33 @@ def test_consistency_stats_match_oracle(olib):
     assert st["first_mismatch"] == -1.0 and st["n_valid"] == 5000
 
 
+def test_consistency_stats_async_matches_sync_bitwise(olib):
+    """rlk_consistency_stats_async: the stream-ordered variant writes the same
+    bits as the synchronous call (same kernels, same fixed order), into device
+    memory, with a caller workspace reused across calls; n = 0 writes the empty
+    result."""
+    import invariant_token_logprob_gb300 as rlk
+    g = np.random.default_rng(9)
+    out = torch.full((8,), float("nan"), dtype=torch.float64, device="cuda")
+    ws = torch.empty(max(16, rlk.stats_workspace_size(100003)), dtype=torch.uint8, device="cuda")
+    for n in (1, 16384, 16385, 100003):
+        b = g.normal(-3, 1, n).astype(np.float32)
+        a = b + (g.normal(0, 1e-3, n) * (g.uniform(size=n) < 0.3)).astype(np.float32)
+        mask = (g.uniform(size=n) > 0.1).astype(np.int8)
+        for mk in (None, mask):
+            ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+            tm = None if mk is None else torch.from_numpy(mk).cuda()
+            rlk.consistency_stats_async(ta, tb, tm, out=out, workspace=ws)
+            got = out.cpu().numpy()
+            ref = np.array([rlk.consistency_stats(ta, tb, tm)[k] for k in rlk.STAT_NAMES])
+            assert np.array_equal(got.view(np.uint64), ref.view(np.uint64)), (n, got, ref)
+            oref = oracle.consistency_stats(a, b, mk, lib=olib)
+            assert got[0] == oref[0] and np.array_equal(got[5:], oref[5:])
+    e = torch.empty(0, device="cuda")
+    rlk.consistency_stats_async(e, e, out=out, workspace=ws)
+    assert out.cpu().tolist() == [0.0] * 7 + [-1.0]
+
+
 def test_chunking_permutation_and_repeat_invariance_small():
     """Bitwise: the tiny workload as one call, in every chunk size 1..64, in a
     permuted order, and repeated, gives identical bits for every row."""
