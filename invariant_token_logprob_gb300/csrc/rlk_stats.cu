@@ -4,15 +4,16 @@
 // |p_rollout - p_train| and the k3 KL estimator r - 1 - log r).
 //
 // d = a - b in double (a = train, b = rollout), r = exp(d), k3 = expm1(d) - d.
-// Every valid position is a summary {count 1, |d|, d, k3, max |d|, bit
-// mismatch, first mismatch index, squared deviation 0}; summaries combine with
-// Chan's pairwise update for the squared deviations about the mean of |d|.
 // Pass 1: block b owns the fixed slice [256 b, 256 b + 256), one position per
-// thread, and combines them in a fixed tree (warp shuffles, then the 8 warps).
-// Pass 2: one block folds block summary j into thread j % 256 in index order,
-// then the same fixed tree.  Same n -> same tree -> same bits.  Slices are
-// small because the double-precision work (expm1 per position) is slow on
-// this GPU: it must be spread over many SMs.
+// thread.  Fixed trees (warp shuffles, then the 8 warps) give the block's
+// count, sum |d|, sum d, sum k3, max |d|, bit mismatches and first mismatch;
+// thread 0 forms the block mean of |d|, and a second tree sums the squared
+// deviations about it.  Pass 2: one warp; lane l folds block summaries l,
+// l + 32, ... in index order with Chan's pairwise update, then a fixed
+// shuffle tree.  Same n -> same trees -> same bits.  The slices are small and
+// the trees use additions (one division per block, one per combination in
+// pass 2) because double precision is slow on this GPU: the work must be
+// spread over many SMs and kept to few operations.
 #include <math.h>
 
 #include "rlk_internal.h"
@@ -34,57 +35,45 @@ __device__ __forceinline__ Part empty_part() {
     return r;
 }
 
-// Combination of two summaries.  Commutative bit for bit (every operation is
-// symmetric in x and y), so shuffle trees need no care about operand order.
+__device__ __forceinline__ double first_of(double x, double y) {
+    return x < 0 ? y : (y < 0 ? x : (x < y ? x : y));
+}
+
+// Chan's pairwise combination.  The squared-deviation term
+// (mean_y - mean_x)^2 n_x n_y / n is formed as t^2 / (n_x n_y n) with
+// t = S_y n_x - S_x n_y (S = sum |d|): one division.  Commutative bit for bit.
 __device__ __forceinline__ Part combine(const Part& x, const Part& y) {
     Part r;
     r.n = x.n + y.n;
     r.m2 = x.m2 + y.m2;
     if (x.n > 0 && y.n > 0) {
-        const double delta = y.sabs / y.n - x.sabs / x.n;
-        r.m2 += delta * delta * (x.n * y.n / r.n);
+        const double t = y.sabs * x.n - x.sabs * y.n;
+        r.m2 += (t * t) / ((x.n * y.n) * r.n);
     }
     r.sabs = x.sabs + y.sabs;
     r.sd = x.sd + y.sd;
     r.sk3 = x.sk3 + y.sk3;
     r.mx = x.mx > y.mx ? x.mx : y.mx;
     r.nmis = x.nmis + y.nmis;
-    r.first = x.first < 0 ? y.first : (y.first < 0 ? x.first : (x.first < y.first ? x.first : y.first));
+    r.first = first_of(x.first, y.first);
     return r;
 }
 
-__device__ __forceinline__ Part shfl_down_part(const Part& v, int off) {
-    Part r;
-    r.n = __shfl_down_sync(0xffffffffu, v.n, off);
-    r.sabs = __shfl_down_sync(0xffffffffu, v.sabs, off);
-    r.sd = __shfl_down_sync(0xffffffffu, v.sd, off);
-    r.sk3 = __shfl_down_sync(0xffffffffu, v.sk3, off);
-    r.mx = __shfl_down_sync(0xffffffffu, v.mx, off);
-    r.nmis = __shfl_down_sync(0xffffffffu, v.nmis, off);
-    r.first = __shfl_down_sync(0xffffffffu, v.first, off);
-    r.m2 = __shfl_down_sync(0xffffffffu, v.m2, off);
-    return r;
+__device__ __forceinline__ double down(double v, int off) {
+    return __shfl_down_sync(0xffffffffu, v, off);
 }
 
-// Fixed tree over the 256 threads' summaries; the result is valid in thread 0.
-__device__ Part block_combine(Part v) {
-    __shared__ Part warp_part[kStatThreads / 32];
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+// Fixed shuffle-down tree sum over the 32 lanes (result in lane 0).
+__device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        const Part o = shfl_down_part(v, off);
-        if (lane < off) v = combine(v, o);
-    }
-    if (lane == 0) warp_part[wid] = v;
-    __syncthreads();
-    if (wid == 0) {
-        v = lane < kStatThreads / 32 ? warp_part[lane] : empty_part();
+    for (int off = 16; off >= 1; off >>= 1) v += down(v, off);
+    return v;
+}
+
+// The same tree over the first 8 lanes.
+__device__ __forceinline__ double warp8_sum(double v) {
 #pragma unroll
-        for (int off = 4; off >= 1; off >>= 1) {
-            const Part o = shfl_down_part(v, off);
-            if (lane < off) v = combine(v, o);
-        }
-    }
+    for (int off = 4; off >= 1; off >>= 1) v += down(v, off);
     return v;
 }
 
@@ -95,32 +84,94 @@ __device__ __forceinline__ bool valid_at(const int8_t* mask, int64_t i) {
 __global__ void __launch_bounds__(kStatThreads)
     stats_block_kernel(const float* __restrict__ a, const float* __restrict__ b,
                        const int8_t* __restrict__ mask, int64_t n, Part* __restrict__ parts) {
+    constexpr int kWarps = kStatThreads / 32;
+    __shared__ double red[7][kWarps];
+    __shared__ double mean_sh;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int64_t i = int64_t(blockIdx.x) * kChunk + threadIdx.x;
-    Part v = empty_part();
+    double cnt = 0, ad = 0, d = 0, k3 = 0, mis = 0, first = -1;
     if (i < n && valid_at(mask, i)) {
         const float fa = a[i], fb = b[i];
-        const double d = double(fa) - double(fb);
-        const double ad = fabs(d);
-        v.n = 1.0;
-        v.sabs = ad;
-        v.sd = d;
-        v.sk3 = expm1(d) - d;
-        v.mx = ad;
+        d = double(fa) - double(fb);
+        ad = fabs(d);
+        cnt = 1;
+        k3 = expm1(d) - d;
         if (__float_as_uint(fa) != __float_as_uint(fb)) {
-            v.nmis = 1.0;
-            v.first = double(i);
+            mis = 1;
+            first = double(i);
         }
     }
-    v = block_combine(v);
-    if (threadIdx.x == 0) parts[blockIdx.x] = v;
+    double mx = ad, fst = first;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const double omx = down(mx, off), ofst = down(fst, off);
+        mx = omx > mx ? omx : mx;
+        fst = first_of(fst, ofst);
+    }
+    double v[5] = {warp_sum(cnt), warp_sum(ad), warp_sum(d), warp_sum(k3), warp_sum(mis)};
+    if (lane == 0) {
+        for (int q = 0; q < 5; ++q) red[q][wid] = v[q];
+        red[5][wid] = mx;
+        red[6][wid] = fst;
+    }
+    __syncthreads();
+    Part pr = empty_part();
+    if (wid == 0) {
+        double w[5];
+        for (int q = 0; q < 5; ++q) w[q] = warp8_sum(lane < kWarps ? red[q][lane] : 0.0);
+        double bmx = lane < kWarps ? red[5][lane] : 0.0;
+        double bfst = lane < kWarps ? red[6][lane] : -1.0;
+#pragma unroll
+        for (int off = 4; off >= 1; off >>= 1) {
+            const double omx = down(bmx, off), ofst = down(bfst, off);
+            bmx = omx > bmx ? omx : bmx;
+            bfst = first_of(bfst, ofst);
+        }
+        if (lane == 0) {
+            pr.n = w[0];
+            pr.sabs = w[1];
+            pr.sd = w[2];
+            pr.sk3 = w[3];
+            pr.nmis = w[4];
+            pr.mx = bmx;
+            pr.first = bfst;
+            mean_sh = w[0] > 0 ? w[1] / w[0] : 0.0;
+        }
+    }
+    __syncthreads();
+    const double dev = cnt > 0 ? (ad - mean_sh) * (ad - mean_sh) : 0.0;
+    const double m2w = warp_sum(dev);
+    if (lane == 0) red[0][wid] = m2w;
+    __syncthreads();
+    if (wid == 0) {
+        const double m2 = warp8_sum(lane < kWarps ? red[0][lane] : 0.0);
+        if (lane == 0) {
+            pr.m2 = m2;
+            parts[blockIdx.x] = pr;
+        }
+    }
 }
 
-__global__ void __launch_bounds__(kStatThreads)
+// One warp.
+__global__ void __launch_bounds__(32)
     stats_final_kernel(const Part* __restrict__ parts, int64_t nblk, double* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
     Part v = empty_part();
-    for (int64_t j = threadIdx.x; j < nblk; j += kStatThreads) v = combine(v, parts[j]);
-    v = block_combine(v);
-    if (threadIdx.x == 0) {
+    for (int64_t j = lane; j < nblk; j += 32) v = combine(v, parts[j]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        Part o;
+        o.n = down(v.n, off);
+        o.sabs = down(v.sabs, off);
+        o.sd = down(v.sd, off);
+        o.sk3 = down(v.sk3, off);
+        o.mx = down(v.mx, off);
+        o.nmis = down(v.nmis, off);
+        o.first = down(v.first, off);
+        o.m2 = down(v.m2, off);
+        if (lane < off) v = combine(v, o);
+    }
+    if (lane == 0) {
         out[0] = v.mx;
         out[1] = v.n > 0 ? v.sabs / v.n : 0.0;
         out[2] = v.n > 0 ? sqrt(v.m2 / v.n) : 0.0;
@@ -151,7 +202,7 @@ cudaError_t launch_consistency_stats(const float* a, const float* b, const int8_
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    stats_final_kernel<<<1, kStatThreads, 0, stream>>>(parts, nblk, device_out);
+    stats_final_kernel<<<1, 32, 0, stream>>>(parts, nblk, device_out);
     return cudaGetLastError();
 }
 
