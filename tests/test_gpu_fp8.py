@@ -63,7 +63,7 @@ def test_packed_weight_codes_are_bit_exact_and_padded_with_zeros(olib):
 
 
 @pytest.mark.parametrize("T,H,V,seed", [(64, 256, 1024, 1), (3, 128, 777, 2), (130, 512, 3001, 3),
-                                        (2, 4096, 151936, 4)])
+                                        (2, 4096, 151936, 4), (300, 384, 2049, 5)])
 def test_fp8_logprob_matches_oracle(T, H, V, seed, olib):
     import invariant_token_logprob_gb300 as rlk
     d = to_dev(lm_head_inputs(T, H, V, seed=seed))
@@ -88,6 +88,23 @@ def test_fp8_batch_invariance_small():
                                      d["targets"][i:i + c].contiguous())) for i in range(0, 64, c)]
         got = tuple(np.concatenate([p[k] for p in parts]) for k in range(3))
         assert_bitwise(full, got, f"fp8 chunk={c}")
+
+
+def test_fp8_pair_and_single_cta_calls_agree_bitwise():
+    """T = 300 runs as CTA pairs (two row tiles per unit; the odd tile of the
+    last unit lies past the padded h and is not copied), H = 384 gives an odd
+    number of 128-element k-blocks (a half-filled last stage), V = 2049 a
+    one-column last vocabulary tile whose odd half is not copied.  Chunks of
+    at most 128 rows run as single CTAs: every row's bits must agree."""
+    import invariant_token_logprob_gb300 as rlk
+    d = to_dev(lm_head_inputs(300, 384, 2049, seed=21))
+    wq, ws = rlk.quantize_fp8_weight(d["W"])
+    full = _np(rlk.logprob_fp8(d["h"], wq, ws, d["targets"]))
+    for c in (1, 100, 128, 129, 150):
+        parts = [_np(rlk.logprob_fp8(d["h"][i:i + c].contiguous(), wq, ws,
+                                     d["targets"][i:i + c].contiguous())) for i in range(0, 300, c)]
+        got = tuple(np.concatenate([p[k] for p in parts]) for k in range(3))
+        assert_bitwise(full, got, f"fp8 T=300 chunk={c}")
 
 
 @pytest.mark.slow

@@ -175,6 +175,27 @@ def test_consistency_stats_match_oracle(olib):
     assert st["first_mismatch"] == -1.0 and st["n_valid"] == 5000
 
 
+@pytest.mark.parametrize("H", [136, 320])
+def test_pair_and_single_cta_calls_agree_bitwise(H, olib):
+    """T = 300 runs as CTA pairs: units of two row tiles, the odd tile of the
+    last unit past the end of h (not copied), H = 136 / 320 an odd number of
+    64-element k-blocks (3 / 5: a half-filled last stage), V = 3001 a ragged
+    last vocabulary tile whose odd half is not copied.  Chunks of at most 128
+    rows run as single CTAs; chunks of 129+ rows as pairs again.  Every row's
+    bits must agree across all of them, and a sample matches the oracle."""
+    d = lm_head_inputs(300, H, 3001, seed=22 + H, hidden="normal", w_std=0.05)
+    dd = to_dev(d)
+    full = gpu_logprob(dd["h"], dd["W"], dd["targets"])
+    for c in (1, 64, 128, 129, 150, 299):
+        parts = [gpu_logprob(dd["h"][i:i + c].contiguous(), dd["W"],
+                             dd["targets"][i:i + c].contiguous()) for i in range(0, 300, c)]
+        got = tuple(np.concatenate([p[k] for p in parts]) for k in range(3))
+        assert_bitwise(full, got, f"H={H} chunk={c}")
+    rows = np.array([0, 127, 128, 255, 256, 299])
+    ref = oracle.logprob(d["h"][rows], d["W"], d["targets"][rows], lib=olib)
+    assert_parity(tuple(x[rows] for x in full), ref, what=f"H={H} sampled rows")
+
+
 def test_consistency_stats_async_matches_sync_bitwise(olib):
     """rlk_consistency_stats_async: the stream-ordered variant writes the same
     bits as the synchronous call (same kernels, same fixed order), into device
