@@ -22,7 +22,9 @@ host buffers (H2D of h and targets, D2H of logp/lse/argmax and the 8
 statistics inside the timed region; W stays resident as model weights do), the dominant kernel's roofline from live CUDA events, SM
 clocks sampled during the timed region, the CPU oracle's throughput on a
 bounded sample, decode-regime points (T = 1..256: HBM-bound at small T), the
-backward (rlk_logprob_backward on the same batch) and the FP8 (W8A8) variant.
+backward (rlk_logprob_backward on the same batch), the FP8 (W8A8) variant, the
+entropy path and the vocabulary-sharded phases (R = 2, 3, 6 shards emulated on
+one GPU).
 
 --impl reference times the fp64 CPU oracle (the only reference this method
 has) on the host cores, each step a bounded sample of the same workload.
@@ -60,6 +62,8 @@ def parse():
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-backward", action="store_true")
     p.add_argument("--no-fp8", action="store_true")
+    p.add_argument("--no-entropy", action="store_true")
+    p.add_argument("--no-shard", action="store_true")
     p.add_argument("--decode-only", action="store_true",
                    help="time only the decode regime at T = --decode-T (for profiling)")
     p.add_argument("--decode-T", type=int, default=1)
@@ -333,6 +337,87 @@ def backward_point(rlk, torch, h, W, tg, pk, reps=10):
                 note="flops = 3 x 2*T*H*V (recompute, dz.W, dz^T.h); peak = bf16 burst")
 
 
+def entropy_point(rlk, torch, h, W, tg, pk, reps=10):
+    """rlk_logprob_entropy on the same batch (T=4096): the forward kernel with the
+    entropy epilogue plus the entropy merge, against the bf16 peak; its logp / lse
+    / argmax must be the forward's bits."""
+    T, H = h.shape
+    V = W.shape[0]
+    ws = torch.empty(rlk.entropy_workspace_size(T, H, V), dtype=torch.uint8, device=h.device)
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        res = rlk.logprob_entropy(h, W, tg, 1.0, workspace=ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        res = rlk.logprob_entropy(h, W, tg, 1.0, workspace=ws)
+    e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / reps * 1e-3
+    fwd = rlk.logprob(h, W, tg, 1.0)
+    same = all(torch.equal(a.view(torch.int32), b.view(torch.int32)) for a, b in zip(res[:3], fwd))
+    rlk.check_device_error()
+    fl = 2.0 * T * H * V
+    return dict(tokens_per_s=T / t, ms_per_call=t * 1e3, tflops=fl / t / 1e12,
+                frac=fl / t / 1e12 / pk["bf16_tflops"], logp_bits_equal_forward=bool(same),
+                mean_entropy=float(res[3].mean().item()))
+
+
+def shard_points(rlk, torch, h, W, tg, pk, Rs=(2, 3, 6), reps=10):
+    """Vocabulary-sharded (tensor-parallel) phases emulated on one GPU at T=4096:
+    R shards of whole 256-column tiles (594 = R x tiles per shard for R = 2, 3, 6),
+    each shard's partials on its own W slice, then the shard-count-invariant merge
+    over the stacked records (what an all-gather would deliver).  Per R: one
+    shard's partials (the per-rank work of an R-way split) against the bf16 peak,
+    the merge, and whether the merged bits equal the unsharded call."""
+    T, H = h.shape
+    V = W.shape[0]
+    bn = rlk.vocab_tile()
+    nvt = (V + bn - 1) // bn
+    stream = torch.cuda.current_stream()
+    full = rlk.logprob(h, W, tg, 1.0)
+
+    def timed(fn, n):
+        for _ in range(2):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n * 1e-3
+
+    res = {}
+    for R in Rs:
+        if nvt % R:
+            continue
+        nvt_s = nvt // R
+        bounds = [(r * nvt_s * bn, min((r + 1) * nvt_s * bn, V)) for r in range(R)]
+        slices = [W[lo:hi].contiguous() for lo, hi in bounds]
+        buf = torch.empty((R, T, nvt_s, 4), dtype=torch.float32, device=h.device)
+
+        def shard(r):
+            rlk.logprob_partials_shard(h, slices[r], tg, V, bounds[r][0], 1.0, out=buf[r])
+
+        t_shard = timed(lambda: shard(0), reps)
+        for r in range(R):
+            shard(r)
+        t_merge = timed(lambda: rlk.lse_merge_sharded(buf, tg, V), reps)
+        got = rlk.lse_merge_sharded(buf, tg, V)
+        same = all(torch.equal(a.view(torch.int32), b.view(torch.int32)) for a, b in zip(got, full))
+        rows = bounds[0][1] - bounds[0][0]
+        fl = 2.0 * T * H * rows
+        res[f"R{R}"] = dict(shard_partials_ms=t_shard * 1e3, shard_tflops=fl / t_shard / 1e12,
+                            shard_frac=fl / t_shard / 1e12 / pk["bf16_tflops"],
+                            merge_ms=t_merge * 1e3, bitwise_equal_unsharded=bool(same))
+        del slices, buf
+    rlk.check_device_error()
+    return res
+
+
 def fp8_points(rlk, torch, h, W, tg, pk, reps=20):
     """The FP8 (W8A8) variant on the same batch: whole rlk_logprob_fp8 call
     (per-token quantisation of h, e4m3 LM-head kernel, merge) at T=4096 against
@@ -525,6 +610,8 @@ def run_ours(args):
     fp8 = None
     if not args.no_fp8:
         fp8 = fp8_points(rlk, torch, h, W, tg, pk)
+    entropy = None if args.no_entropy else entropy_point(rlk, torch, h, W, tg, pk)
+    sharded = None if args.no_shard else shard_points(rlk, torch, h, W, tg, pk)
 
     if rank != 0:
         return 0
@@ -558,7 +645,7 @@ def run_ours(args):
                 clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"],
                             reasons=clk["reasons"], samples=clk["samples"],
                             window=clk.get("window")),
-                decode=decode, backward=backward, fp8=fp8,
+                decode=decode, backward=backward, fp8=fp8, entropy=entropy, sharded=sharded,
                 bitwise_mismatch_vs_first_call=mism)
     print(json.dumps(line), flush=True)
     return 0
