@@ -568,37 +568,81 @@ def run_ours(args):
     value = tokens / elapsed
 
     # ---------------------------------------------------------------- e2e
+    # Through the public calls (rlk_logprob + rlk_consistency_stats_async), run
+    # the way a training or serving loop runs them: step i+1's inputs are copied
+    # from pinned host memory on a copy stream while step i computes, and step
+    # i's results (logp, lse, argmax and the 8 statistics) are copied back on
+    # the copy stream and read on the host during step i+1.  Every step moves its
+    # own bytes both ways inside the timed region; the last step's results are
+    # waited for before the clock stops.
+    f32, i32 = torch.float32, torch.int32
     h_host = h.cpu().pin_memory()
     tg_host = tg.cpu().pin_memory()
-    outs_host = [torch.empty(T, dtype=dt).pin_memory() for dt in (torch.float32, torch.float32, torch.int32)]
-    stats_host = torch.empty(8, dtype=torch.float64).pin_memory()
-    h_dev = torch.empty_like(h)
-    tg_dev = torch.empty_like(tg)
+    NB = 2  # double-buffered device inputs / outputs
+    h_dev = [torch.empty_like(h) for _ in range(NB)]
+    tg_dev = [torch.empty_like(tg) for _ in range(NB)]
+    outs_dev = [[torch.empty(T, device=dev, dtype=dt) for dt in (f32, f32, i32)] for _ in range(NB)]
+    st_dev = [torch.empty(8, dtype=torch.float64, device=dev) for _ in range(NB)]
+    outs_host = [[torch.empty(T, dtype=dt).pin_memory() for dt in (f32, f32, i32)]
+                 for _ in range(NB)]
+    st_host = [torch.empty(8, dtype=torch.float64).pin_memory() for _ in range(NB)]
+    copy_stream = torch.cuda.Stream(dev)
+    h2d_done = [torch.cuda.Event() for _ in range(NB)]
+    computed = [torch.cuda.Event() for _ in range(NB)]
+    d2h_done = [torch.cuda.Event() for _ in range(NB)]
+    e2e_mism = [0]
+
+    def h2d(b):
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(computed[b])  # the step that last used buffer b
+            h_dev[b].copy_(h_host, non_blocking=True)
+            tg_dev[b].copy_(tg_host, non_blocking=True)
+            h2d_done[b].record(copy_stream)
+
+    def compute_and_d2h(b):
+        stream.wait_event(h2d_done[b])
+        stream.wait_event(d2h_done[b])  # its previous results have left the device
+        lp, lse, am = rlk.logprob(h_dev[b], W, tg_dev[b], 1.0, out=outs_dev[b])
+        rlk.consistency_stats_async(lp, rollout, mask, out=st_dev[b], workspace=stats_ws)
+        computed[b].record(stream)
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(computed[b])
+            for o, oh in zip(outs_dev[b], outs_host[b]):
+                oh.copy_(o, non_blocking=True)
+            st_host[b].copy_(st_dev[b], non_blocking=True)
+            d2h_done[b].record(copy_stream)
+
+    def read_host(b):
+        d2h_done[b].synchronize()
+        e2e_mism[0] += int(st_host[b][6].item())
+
+    def e2e_run(n):
+        h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                h2d((i + 1) % NB)
+            compute_and_d2h(i % NB)
+            if i >= 1:
+                read_host((i - 1) % NB)
+        read_host((n - 1) % NB)
+
     e2e_steps = max(3, min(args.steps, 100))
-
-    def e2e_step():
-        h_dev.copy_(h_host, non_blocking=True)
-        tg_dev.copy_(tg_host, non_blocking=True)
-        lp, lse, am = rlk.logprob(h_dev, W, tg_dev, 1.0, out=out)
-        rlk.consistency_stats_async(lp, rollout, mask, out=stats_rows[0], workspace=stats_ws)
-        for o, oh in zip((lp, lse, am), outs_host):
-            oh.copy_(o, non_blocking=True)
-        stats_host.copy_(stats_rows[0], non_blocking=True)
-        stream.synchronize()
-
-    for _ in range(3):
-        e2e_step()
+    e2e_run(3)
     barrier(world)
     torch.cuda.synchronize()
+    e2e_mism[0] = 0
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_run(e2e_steps)
     e2e_el = max_over_ranks(time.perf_counter() - t0, world, dev)
-    assert np.array_equal(outs_host[0].numpy().view(np.uint32), out[0].cpu().numpy().view(np.uint32))
-    assert stats_host[6].item() == 0, "e2e outputs drifted from the device-timed steps"
+    last = (e2e_steps - 1) % NB
+    assert np.array_equal(outs_host[last][0].numpy().view(np.uint32),
+                          out[0].cpu().numpy().view(np.uint32))
+    assert e2e_mism[0] == 0, "e2e outputs drifted from the device-timed steps"
     e2e = dict(value=T * e2e_steps * world / e2e_el, unit="tokens/s",
                h2d_bytes_per_step=int(h.numel() * 2 + tg.numel() * 4),
-               d2h_bytes_per_step=int(T * 12 + 8 * 8))
+               d2h_bytes_per_step=int(T * 12 + 8 * 8),
+               pipeline="inputs of step i+1 copied while step i computes; results of step i "
+                        "read on the host during step i+1")
 
     # ---------------------------------------------------------------- regimes
     decode = None
