@@ -63,7 +63,7 @@ def test_bounded_wait_runs_out_and_context_survives(olib):
     assert_parity(gpu, oracle.logprob(d["h"], d["W"], d["targets"], lib=olib), what="after timeout")
 
 
-@pytest.mark.parametrize("T", [1, 37])
+@pytest.mark.parametrize("T", [1, 37, 300])  # 300: CTA-pair clusters, ragged last unit
 def test_cuda_graph_capture_and_replay(T):
     import invariant_token_logprob_gb300 as rlk
     H, V = 256, 3000
