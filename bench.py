@@ -33,6 +33,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -82,9 +83,15 @@ def peaks():
 
 
 def kernel_hash():
+    """Hash of the LM-head kernel's code: comments and whitespace are dropped, so
+    only a change that can change the compiled kernel invalidates recorded
+    counters."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, rel), "rb").read())
+        src = open(os.path.join(ROOT, rel), encoding="utf-8").read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

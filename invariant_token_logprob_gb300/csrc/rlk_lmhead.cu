@@ -20,12 +20,20 @@
 // row (TMEM lane) it occupies, rows never mix, and which CTA processes a tile
 // only changes when it is done, not how.
 //
-// Structure: one persistent CTA per SM (grid = min(#tiles, #SMs)), 6 warps:
-//   warp 0      TMA producer: h and W k-blocks into a 4-stage smem ring
-//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=16) per stage;
-//               also allocates / frees the 512 TMEM columns
+// Structure: persistent, one CTA per SM, 6 warps:
+//   warp 0      TMA producer: h and W k-blocks into a shared-memory ring
+//   warp 1      MMA issuer (tcgen05.mma, N=256, K=16 bf16 / 32 e4m3); also
+//               allocates / frees the 512 TMEM columns
 //   warps 2..5  epilogue: TMEM -> registers -> partial record; one thread per
 //               row, warp w reads TMEM lanes 32*(w%4) .. +31
+// Two launch shapes (template parameter kPair), chosen by the number of rows:
+//   single CTA (T <= 128): M=128, a 4-stage ring of 48 KB (one k-block:
+//     h 16 KB + W 32 KB), grid = min(#tiles, #SMs);
+//   CTA pair (T > 128): clusters of 2, tcgen05 cta_group::2 with M=256 issued
+//     by the even CTA, each CTA staging its own 128 h rows and half of the W
+//     block; a 3-stage ring of 64 KB holding two k-blocks per stage (one
+//     barrier round and one commit per 8 MMAs); grid sized by the occupancy
+//     of clusters.
 // The accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue
 // of tile i overlaps the MMAs of tile i+1.  Every wait is bounded in time.
 #include <cuda_bf16.h>
@@ -52,9 +60,13 @@ constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kThreads = 192;
 
 // Per-CTA pipeline shape.  Single CTA: the CTA stages a 128-row h block and the
-// whole 256-row W block of each k-block.  CTA pair: the even CTA's MMA (M = 256)
-// covers both CTAs' 128-row h blocks, and each CTA stages half (128 rows) of the
-// W block, so a stage is 32 KiB instead of 48 and six stages fit.
+// whole 256-row W block of each k-block (48 KiB), one k-block per stage, four
+// stages.  CTA pair: the even CTA's MMA (M = 256) covers both CTAs' 128-row h
+// blocks, and each CTA stages half (128 rows) of the W block, so a k-block is
+// 32 KiB; a stage holds two k-blocks, three stages.  Two k-blocks per stage
+// halve the barrier rounds and commits per MMA, which measured ~8% fewer cycles
+// than six one-k-block stages in the compute-bound regime; in the weight-
+// streaming (decode) regime the single CTA's smaller stages measured better.
 template <bool kPair>
 struct Pipe {
     static constexpr int kBRows = kPair ? kBN / 2 : kBN;  // W rows one CTA stages
