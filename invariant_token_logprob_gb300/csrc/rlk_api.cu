@@ -163,7 +163,7 @@ rlk_status prepare_maps(const void* h, const void* W, int64_t T, int64_t H, int6
         h = pad_buf;
         h_rows = rlk::kMinTmaRows;
     }
-    if (!encode_bf16_2d(th, h, h_rows, H, kRowTile) ||
+    if (!encode_bf16_2d(th, h, h_rows, H, rlk::lmhead_a_box_rows(T)) ||
         !encode_bf16_2d(tw, W, V, H, rlk::lmhead_w_box_rows(T)))
         return RLK_ERR_CUDA;
     return RLK_OK;
@@ -372,9 +372,13 @@ rlk_status rlk_quantize_fp8_rows(const void* x_bf16, int64_t rows, int64_t H, ui
 }
 
 namespace {
-// The quantised h is padded with zero rows to whole 128-row tiles, so no TMA box
-// of it reaches past its end (zero codes either way: no result bit changes).
-int64_t fp8_h_rows(int64_t T) { return (T + kRowTile - 1) / kRowTile * kRowTile; }
+// The quantised h is padded with zero rows to whole h boxes (128-row tiles for
+// CTA pairs, 16-row multiples for single-CTA calls), so no TMA box of it reaches
+// past its end (zero codes either way: no result bit changes).
+int64_t fp8_h_rows(int64_t T) {
+    const int64_t box = rlk::lmhead_a_box_rows(T);
+    return (T + box - 1) / box * box;
+}
 size_t round16(size_t b) { return (b + 15) / 16 * 16; }
 }  // namespace
 
@@ -429,7 +433,7 @@ rlk_status rlk_logprob_fp8(const void* hidden_bf16, const uint8_t* weight_e4m3,
     CUtensorMap th, tw;
     // the packed weight as rows of 128 bytes: blocks * kVocabTile of them
     const int64_t packed_rows = num_vocab_tiles(V) * (H / 128) * kVocabTile;
-    if (!encode_2d(&th, qh, hrows, H, kRowTile, true) ||
+    if (!encode_2d(&th, qh, hrows, H, rlk::lmhead_a_box_rows(T), true) ||
         !encode_2d(&tw, weight_e4m3, packed_rows, 128, rlk::lmhead_w_box_rows(T), true))
         return RLK_ERR_CUDA;
     e = rlk::launch_lmhead_partials_fp8(&th, &tw, targets_i32, sh, weight_scales_f32, workspace, T,

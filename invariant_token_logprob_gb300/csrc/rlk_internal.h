@@ -20,6 +20,12 @@ constexpr int kKBlock = 64;      // K elements per pipeline stage (one 128-B swi
 // height must equal.
 bool lmhead_use_pair(int64_t T);
 int lmhead_w_box_rows(int64_t T);
+// Rows of the h box the kernel copies per k-block, which the h tensor map's box
+// height must equal: the whole 128-row tile for CTA pairs; for single-CTA calls
+// (T <= 128) the call's rows rounded up to a multiple of 16 (at least 16).  The
+// MMA still reads a 128-row operand; rows past the box hold whatever the shared
+// memory held and are never reported.
+int lmhead_a_box_rows(int64_t T);
 
 // Calls with fewer rows than this get their h rows copied into a zero-padded
 // buffer of this many rows before the LM-head kernel runs (see rlk_pad.cu).

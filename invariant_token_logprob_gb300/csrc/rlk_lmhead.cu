@@ -47,6 +47,11 @@ namespace rlk {
 
 bool lmhead_use_pair(int64_t T) { return T > kRowTile; }
 int lmhead_w_box_rows(int64_t T) { return lmhead_use_pair(T) ? kVocabTile / 2 : kVocabTile; }
+int lmhead_a_box_rows(int64_t T) {
+    if (lmhead_use_pair(T)) return kRowTile;
+    const int64_t r = (T + kMinTmaRows - 1) / kMinTmaRows * kMinTmaRows;
+    return int(r < kMinTmaRows ? kMinTmaRows : r);
+}
 
 namespace {
 
@@ -101,6 +106,7 @@ struct Args {
     uint16_t* dz;          // mode 1: [T][V] bf16 gradient of logp w.r.t. the logits
     int64_t T;
     int64_t h_rows; // rows the h tensor map covers (>= T; padded copies are longer)
+    int a_rows;     // rows of each h box (lmhead_a_box_rows(T))
     int V;          // columns of the W this launch sees (a shard's rows when sharded)
     int col_offset; // global vocabulary index of that W's row 0 (0 unless sharded)
     int num_m;   // row tiles
@@ -287,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tile of the last unit) or of W (odd half of the last vocabulary
                 // tile) is not copied; the MMA then reads stale shared memory for
                 // rows / columns that the epilogues never report.
-                uint32_t kb_bytes = P::kKbBytes;  // per k-block, both CTAs of a pair
+                // per k-block: single CTA, its h box and W block; CTA pair, both CTAs
+                uint32_t kb_bytes = uint32_t(p.a_rows) * 128u + P::kBBytes;
                 bool load_a = true, load_b = true;
                 if constexpr (kPair) {
                     kb_bytes = 0;
@@ -680,6 +687,7 @@ template <int kMode, bool kFp8 = false>
 cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, int64_t H,
                         int num_sms, cudaStream_t stream) {
     if (a.h_rows == 0) a.h_rows = a.T;
+    a.a_rows = lmhead_a_box_rows(a.T);
     if (lmhead_use_pair(a.T) && !a.stall_selftest)
         return launch_variant<kMode, kFp8, true>(th, tw, a, H, num_sms, stream);
     return launch_variant<kMode, kFp8, false>(th, tw, a, H, num_sms, stream);
