@@ -435,6 +435,18 @@ def fp8_points(rlk, torch, h, W, tg, pk, reps=20):
     wq, wsc = rlk.quantize_fp8_weight(W)
     stream = torch.cuda.current_stream()
     res = {}
+    # the weight quantisation a training step repeats whenever W changes
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(5):
+        rlk.quantize_fp8_weight(W, out=(wq, wsc))
+    e1.record(stream)
+    e1.synchronize()
+    tq = e0.elapsed_time(e1) / 5 * 1e-3
+    qbytes = V * H * 2 + wq.numel() + V * 4
+    res["quantize_weight"] = dict(ms_per_call=tq * 1e3, hbm_gbs=qbytes / tq / 1e9,
+                                  hbm_frac=qbytes / tq / 1e9 / pk["hbm_gbs"])
 
     def timed(hh, tt, n):
         buf = torch.empty(rlk.fp8_workspace_size(hh.shape[0], H, V), dtype=torch.uint8,

@@ -447,14 +447,21 @@ def fp8_workspace_size(T: int, H: int, V: int) -> int:
     return lib().rlk_logprob_fp8_workspace_size(int(T), int(H), int(V))
 
 
-def quantize_fp8_weight(W, stream=None):
+def quantize_fp8_weight(W, out=None, stream=None):
     """rlk_quantize_fp8_weight: bf16 W [V, H] -> (tile-packed e4m3 codes as a flat uint8
-    tensor, f32 scales [V])."""
+    tensor, f32 scales [V]).  Pass out=(packed, scales) to reuse buffers."""
     import torch
     _need(W, torch.bfloat16, "W", 2)
     V, H = W.shape
-    packed = torch.empty(lib().rlk_fp8_weight_bytes(V, H), dtype=torch.uint8, device=W.device)
-    scales = torch.empty(V, dtype=torch.float32, device=W.device)
+    if out is None:
+        packed = torch.empty(lib().rlk_fp8_weight_bytes(V, H), dtype=torch.uint8, device=W.device)
+        scales = torch.empty(V, dtype=torch.float32, device=W.device)
+    else:
+        packed, scales = out
+        _need(packed, torch.uint8, "packed", 1)
+        _need(scales, torch.float32, "scales", 1)
+        if packed.numel() < lib().rlk_fp8_weight_bytes(V, H) or scales.numel() < V:
+            raise ValueError("out buffers too small for rlk_fp8_weight_bytes(V, H) / V")
     _check(lib().rlk_quantize_fp8_weight(_ptr(W), V, H, _ptr(packed), _ptr(scales),
                                          _stream(stream)), "rlk_quantize_fp8_weight")
     return packed, scales

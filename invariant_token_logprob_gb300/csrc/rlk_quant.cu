@@ -6,7 +6,7 @@
 // dense-GEMM and expert-GEMM sections).  Per row r of a bf16 matrix [rows][H]:
 //   s_r  = amax_k |x[r,k]| / 448   (fp32 division; 1 for an all-zero row)
 //   q    = e4m3 RNE of x[r,k] / s_r (fp32 division), saturating at +-448
-// One CTA per row; the max is exact whatever the order, the division is the
+// One warp per row; the max is exact whatever the order, the division is the
 // IEEE one and the conversion is the hardware's RNE cvt, so a row's codes and
 // scale depend only on that row.  Rows out_rows > rows (zero padding for small
 // T) get code 0 and scale 1.
@@ -20,10 +20,8 @@ namespace rlk {
 namespace {
 
 constexpr int kQuantThreads = 256;
+constexpr int kRowsPerCta = kQuantThreads / 32;  // one warp per row
 
-// One CTA per row: the 256 threads share the row's elements, the amax is
-// reduced through warp shuffles and shared memory (a max: exact in any order),
-// and every element is then divided and converted on its own.
 // Byte offset of code (row r, column k) in the output.  Row-major: r*H + k.
 // Tile-packed (the fp8 weight format): rows grouped in vocabulary tiles of
 // kVocabTile, columns in 128-byte k-blocks, each (tile, k-block) a contiguous
@@ -41,79 +39,123 @@ __device__ __forceinline__ int64_t code_offset(int64_t r, int k, int H) {
     }
 }
 
-template <bool kTiled>
-__global__ void __launch_bounds__(kQuantThreads)
-    quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int H,
-                         uint8_t* __restrict__ codes, float* __restrict__ scales,
-                         int64_t scale_rows) {
-    grid_launch_dependents();
-    __shared__ float warp_max[kQuantThreads / 32];
-    const int tid = threadIdx.x;
-    const int64_t r = blockIdx.x;
-    if (r >= rows) {  // zero padding rows (uniform per CTA)
-        for (int k = tid * 16; k < H; k += kQuantThreads * 16)
-            *reinterpret_cast<uint4*>(codes + code_offset<kTiled>(r, k, H)) =
-                make_uint4(0u, 0u, 0u, 0u);
-        if (tid == 0 && r < scale_rows) scales[r] = 1.0f;
-        return;
-    }
-    const __nv_bfloat16* xr = x + r * int64_t(H);
-    float amax = 0.0f;
-    for (int k = tid * 8; k < H; k += kQuantThreads * 8) {  // H % 16 == 0
-        const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
-        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(p[i]);
-            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-        }
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if ((tid & 31) == 0) warp_max[tid >> 5] = amax;
-    __syncthreads();
-    amax = warp_max[0];
-#pragma unroll
-    for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
-    const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    for (int k = tid * 16; k < H; k += kQuantThreads * 16) {
+// x / sc rounded to nearest, from rs = the correctly rounded 1 / sc: the
+// product's residual is exact under fma, and one correction step gives the
+// correctly rounded quotient (Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", 1990).  Zero keeps its sign (the
+// residual of a zero quotient is +0, which would turn -0 into +0).  Callers use
+// it only while rs is finite and normal; the GPU tests check it against the
+// IEEE division for every bf16 x and every scale amax/448 a bf16 amax can give.
+__device__ __forceinline__ float div_by_scale(float x, float sc, float rs) {
+    const float q = __fmul_rn(x, rs);
+    const float e = __fmaf_rn(-q, sc, x);
+    return e == 0.0f ? q : __fmaf_rn(e, rs, q);
+}
+
+template <bool kFast>
+__device__ __forceinline__ float quotient(float x, float sc, float rs) {
+    if constexpr (kFast)
+        return div_by_scale(x, sc, rs);
+    else
+        return __fdiv_rn(x, sc);
+}
+
+template <bool kFast>
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d, float sc, float rs) {
+    const uint32_t c0 = __nv_cvt_float_to_fp8(quotient<kFast>(a, sc, rs), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t c1 = __nv_cvt_float_to_fp8(quotient<kFast>(b, sc, rs), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t c2 = __nv_cvt_float_to_fp8(quotient<kFast>(c, sc, rs), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t c3 = __nv_cvt_float_to_fp8(quotient<kFast>(d, sc, rs), __NV_SATFINITE, __NV_E4M3);
+    return c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+}
+
+// Pass 2 of a row: divide, convert, store 16 codes per lane and step.
+template <bool kTiled, bool kFast>
+__device__ __forceinline__ void convert_row(const __nv_bfloat16* __restrict__ xr, int64_t r, int H,
+                                            int lane, float sc, float rs,
+                                            uint8_t* __restrict__ codes) {
+    for (int k = lane * 16; k < H; k += 32 * 16) {
         uint32_t out[4];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const uint4 v = *reinterpret_cast<const uint4*>(xr + k + half * 8);
             const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-            for (int i = 0; i < 4; i += 2) {
-                const float2 a = __bfloat1622float2(p[i]);
-                const float2 b = __bfloat1622float2(p[i + 1]);
-                const uint32_t c0 = __nv_cvt_float_to_fp8(__fdiv_rn(a.x, sc), __NV_SATFINITE, __NV_E4M3);
-                const uint32_t c1 = __nv_cvt_float_to_fp8(__fdiv_rn(a.y, sc), __NV_SATFINITE, __NV_E4M3);
-                const uint32_t c2 = __nv_cvt_float_to_fp8(__fdiv_rn(b.x, sc), __NV_SATFINITE, __NV_E4M3);
-                const uint32_t c3 = __nv_cvt_float_to_fp8(__fdiv_rn(b.y, sc), __NV_SATFINITE, __NV_E4M3);
-                out[half * 2 + i / 2] = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
-            }
+            const float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
+            const float2 c = __bfloat1622float2(p[2]), d = __bfloat1622float2(p[3]);
+            out[half * 2] = e4m3x4<kFast>(a.x, a.y, b.x, b.y, sc, rs);
+            out[half * 2 + 1] = e4m3x4<kFast>(c.x, c.y, d.x, d.y, sc, rs);
         }
         *reinterpret_cast<uint4*>(codes + code_offset<kTiled>(r, k, H)) =
             make_uint4(out[0], out[1], out[2], out[3]);
     }
-    if (tid == 0) scales[r] = sc;
+}
+
+// One warp per row: lane l owns the 16-element groups l, l + 32, ... (two
+// 16-byte loads each, so a warp reads 1 KB contiguous per step).  Pass 1 takes
+// |x| max over the row and reduces it with shuffles (a max: exact in any
+// order); pass 2 re-reads the row (L1-resident), divides each element by the
+// row scale and converts it.  No block-level synchronisation.  The division
+// takes the reciprocal path for sc >= 2^-64 (a quotient that can reach a
+// nonzero code then has a normal residual), the IEEE division otherwise (rows
+// whose max |x| is below ~1e-17).
+template <bool kTiled>
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t out_rows,
+                         int H, uint8_t* __restrict__ codes, float* __restrict__ scales,
+                         int64_t scale_rows) {
+    grid_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t r = int64_t(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
+    if (r >= out_rows) return;
+    if (r >= rows) {  // zero padding rows
+        for (int k = lane * 16; k < H; k += 32 * 16)
+            *reinterpret_cast<uint4*>(codes + code_offset<kTiled>(r, k, H)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        if (lane == 0 && r < scale_rows) scales[r] = 1.0f;
+        return;
+    }
+    const __nv_bfloat16* xr = x + r * int64_t(H);
+    float amax = 0.0f;
+    for (int k = lane * 16; k < H; k += 32 * 16) {  // H % 16 == 0
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint4 v = *reinterpret_cast<const uint4*>(xr + k + half * 8);
+            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(p[i]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    if (sc >= 0x1p-64f)
+        convert_row<kTiled, true>(xr, r, H, lane, sc, __frcp_rn(sc), codes);
+    else
+        convert_row<kTiled, false>(xr, r, H, lane, sc, 0.0f, codes);
+    if (lane == 0) scales[r] = sc;
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_rows, int64_t H,
                                      void* codes, float* scales, cudaStream_t stream) {
-    quantize_rows_kernel<false><<<unsigned(out_rows), kQuantThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), rows, int(H), static_cast<uint8_t*>(codes), scales,
-        out_rows);
+    const int64_t ctas = (out_rows + kRowsPerCta - 1) / kRowsPerCta;
+    quantize_rows_kernel<false><<<unsigned(ctas), kQuantThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, out_rows, int(H),
+        static_cast<uint8_t*>(codes), scales, out_rows);
     return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_fp8_weight_tiled(const void* W, int64_t V, int64_t H, void* packed,
                                              float* scales, cudaStream_t stream) {
     const int64_t padded = (V + kVocabTile - 1) / kVocabTile * kVocabTile;
-    quantize_rows_kernel<true><<<unsigned(padded), kQuantThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(W), V, int(H), static_cast<uint8_t*>(packed), scales, V);
+    const int64_t ctas = (padded + kRowsPerCta - 1) / kRowsPerCta;
+    quantize_rows_kernel<true><<<unsigned(ctas), kQuantThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(W), V, padded, int(H), static_cast<uint8_t*>(packed),
+        scales, V);
     return cudaGetLastError();
 }
 

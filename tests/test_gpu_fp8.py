@@ -46,6 +46,33 @@ def test_quantiser_codes_and_scales_are_bit_exact(olib):
     assert np.array_equal(codes.cpu().numpy(), rc)
 
 
+def test_quantiser_division_is_ieee_on_its_whole_input_domain():
+    """Exhaustive: a row's scale is s = amax / 448 for a bf16 amax, and its codes
+    are the e4m3 RNE of the fp32 IEEE quotient x / s for bf16 x with |x| <= amax.
+    Every positive finite bf16 amax is taken, each row holding every finite bf16
+    value with |x| <= amax (the others replaced by 0, so the row's amax is
+    exactly that value): about 2.1e9 (x, s) pairs.  The reference is torch's
+    division by a device tensor (true IEEE division) and its float8 e4m3 cast,
+    computed on the same device; scales and codes must match bit for bit, signed
+    zeros included."""
+    import invariant_token_logprob_gb300 as rlk
+    pat = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    base = torch.where(torch.isfinite(pat.float()), pat, torch.zeros_like(pat)).cuda()
+    mags = pat[1:0x7F80].float().cuda()  # every positive finite bf16 value, ascending
+    absb = base.float().abs()
+    for c0 in range(0, mags.numel(), 512):
+        amax = mags[c0:c0 + 512]
+        rows = torch.where(absb[None, :] <= amax[:, None], base[None, :],
+                           torch.zeros_like(base)[None, :]).contiguous()
+        codes, scales = rlk.quantize_fp8_rows(rows)
+        ref_s = amax / torch.full_like(amax, 448.0)
+        assert torch.equal(scales.view(torch.int32), ref_s.view(torch.int32)), c0
+        ref = (rows.float() / scales[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        bad = (codes != ref).nonzero()
+        assert bad.numel() == 0, (c0, bad[:5].tolist())
+    rlk.check_device_error()
+
+
 def test_packed_weight_codes_are_bit_exact_and_padded_with_zeros(olib):
     """The tile-packed fp8 weight holds the oracle's row codes (after unpacking)
     and zero codes in the padding rows of the last vocabulary tile."""
