@@ -58,7 +58,6 @@ namespace {
 constexpr int kBM = kRowTile;
 constexpr int kBN = kVocabTile;
 constexpr int kBK = kKBlock;
-constexpr int kUK = 16;  // K per tcgen05.mma kind::f16
 constexpr int kAccBufs = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
