@@ -6,7 +6,7 @@
 // dense-GEMM and expert-GEMM sections).  Per row r of a bf16 matrix [rows][H]:
 //   s_r  = amax_k |x[r,k]| / 448   (fp32 division; 1 for an all-zero row)
 //   q    = e4m3 RNE of x[r,k] / s_r (fp32 division), saturating at +-448
-// One warp per row; the max is exact whatever the order, the division is the
+// A warp or a CTA per row; the max is exact whatever the order, the division is the
 // IEEE one and the conversion is the hardware's RNE cvt, so a row's codes and
 // scale depend only on that row.  Rows out_rows > rows (zero padding for small
 // T) get code 0 and scale 1.
@@ -20,7 +20,6 @@ namespace rlk {
 namespace {
 
 constexpr int kQuantThreads = 256;
-constexpr int kRowsPerCta = kQuantThreads / 32;  // one warp per row
 
 // Byte offset of code (row r, column k) in the output.  Row-major: r*H + k.
 // Tile-packed (the fp8 weight format): rows grouped in vocabulary tiles of
@@ -69,12 +68,12 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d, f
     return c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
 }
 
-// Pass 2 of a row: divide, convert, store 16 codes per lane and step.
-template <bool kTiled, bool kFast>
+// Pass 2 of a row: divide, convert, store 16 codes per thread and step.
+template <bool kTiled, bool kFast, int kTpr>
 __device__ __forceinline__ void convert_row(const __nv_bfloat16* __restrict__ xr, int64_t r, int H,
-                                            int lane, float sc, float rs,
+                                            int t, float sc, float rs,
                                             uint8_t* __restrict__ codes) {
-    for (int k = lane * 16; k < H; k += 32 * 16) {
+    for (int k = t * 16; k < H; k += kTpr * 16) {
         uint32_t out[4];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -90,33 +89,36 @@ __device__ __forceinline__ void convert_row(const __nv_bfloat16* __restrict__ xr
     }
 }
 
-// One warp per row: lane l owns the 16-element groups l, l + 32, ... (two
-// 16-byte loads each, so a warp reads 1 KB contiguous per step).  Pass 1 takes
-// |x| max over the row and reduces it with shuffles (a max: exact in any
-// order); pass 2 re-reads the row (L1-resident), divides each element by the
-// row scale and converts it.  No block-level synchronisation.  The division
+// kTpr threads per row: 32 (one warp; many rows, as for W) or 256 (one CTA;
+// few rows, as for a decode step's h, where the latency of one row counts).
+// Thread t of a row owns the 16-element groups t, t + kTpr, ... (two 16-byte
+// loads each, so a warp reads 1 KB contiguous per step).  Pass 1 takes |x| max
+// over the row, reduced through shuffles (and shared memory across the CTA's
+// warps when kTpr = 256; a max: exact in any order); pass 2 re-reads the row,
+// divides each element by the row scale and converts it.  The division
 // takes the reciprocal path for sc >= 2^-64 (a quotient that can reach a
 // nonzero code then has a normal residual), the IEEE division otherwise (rows
 // whose max |x| is below ~1e-17).
-template <bool kTiled>
+template <bool kTiled, int kTpr>
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t out_rows,
                          int H, uint8_t* __restrict__ codes, float* __restrict__ scales,
                          int64_t scale_rows) {
+    static_assert(kTpr == 32 || kTpr == kQuantThreads, "a warp or the whole CTA per row");
     grid_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int64_t r = int64_t(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
-    if (r >= out_rows) return;
-    if (r >= rows) {  // zero padding rows
-        for (int k = lane * 16; k < H; k += 32 * 16)
+    const int t = threadIdx.x % kTpr;
+    const int64_t r = int64_t(blockIdx.x) * (kQuantThreads / kTpr) + threadIdx.x / kTpr;
+    if (r >= out_rows) return;  // uniform per row group (warp or CTA)
+    if (r >= rows) {            // zero padding rows
+        for (int k = t * 16; k < H; k += kTpr * 16)
             *reinterpret_cast<uint4*>(codes + code_offset<kTiled>(r, k, H)) =
                 make_uint4(0u, 0u, 0u, 0u);
-        if (lane == 0 && r < scale_rows) scales[r] = 1.0f;
+        if (t == 0 && r < scale_rows) scales[r] = 1.0f;
         return;
     }
     const __nv_bfloat16* xr = x + r * int64_t(H);
     float amax = 0.0f;
-    for (int k = lane * 16; k < H; k += 32 * 16) {  // H % 16 == 0
+    for (int k = t * 16; k < H; k += kTpr * 16) {  // H % 16 == 0
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const uint4 v = *reinterpret_cast<const uint4*>(xr + k + half * 8);
@@ -130,20 +132,28 @@ __global__ void __launch_bounds__(kQuantThreads)
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if constexpr (kTpr == kQuantThreads) {
+        __shared__ float warp_max[kQuantThreads / 32];
+        if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
+        __syncthreads();
+        amax = warp_max[0];
+#pragma unroll
+        for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+    }
     const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
     if (sc >= 0x1p-64f)
-        convert_row<kTiled, true>(xr, r, H, lane, sc, __frcp_rn(sc), codes);
+        convert_row<kTiled, true, kTpr>(xr, r, H, t, sc, __frcp_rn(sc), codes);
     else
-        convert_row<kTiled, false>(xr, r, H, lane, sc, 0.0f, codes);
-    if (lane == 0) scales[r] = sc;
+        convert_row<kTiled, false, kTpr>(xr, r, H, t, sc, 0.0f, codes);
+    if (t == 0) scales[r] = sc;
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_rows, int64_t H,
                                      void* codes, float* scales, cudaStream_t stream) {
-    const int64_t ctas = (out_rows + kRowsPerCta - 1) / kRowsPerCta;
-    quantize_rows_kernel<false><<<unsigned(ctas), kQuantThreads, 0, stream>>>(
+    // one CTA per row: a decode step quantises a handful of rows and waits for it
+    quantize_rows_kernel<false, kQuantThreads><<<unsigned(out_rows), kQuantThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(x), rows, out_rows, int(H),
         static_cast<uint8_t*>(codes), scales, out_rows);
     return cudaGetLastError();
@@ -152,8 +162,9 @@ cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_ro
 cudaError_t launch_quantize_fp8_weight_tiled(const void* W, int64_t V, int64_t H, void* packed,
                                              float* scales, cudaStream_t stream) {
     const int64_t padded = (V + kVocabTile - 1) / kVocabTile * kVocabTile;
+    constexpr int kRowsPerCta = kQuantThreads / 32;  // one warp per row
     const int64_t ctas = (padded + kRowsPerCta - 1) / kRowsPerCta;
-    quantize_rows_kernel<true><<<unsigned(ctas), kQuantThreads, 0, stream>>>(
+    quantize_rows_kernel<true, 32><<<unsigned(ctas), kQuantThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(W), V, padded, int(H), static_cast<uint8_t*>(packed),
         scales, V);
     return cudaGetLastError();
