@@ -42,6 +42,10 @@
  *     default stream) and perform no host synchronisation, unless stated.
  *   - Requires a compute-capability 10.3 device (GB300); otherwise
  *     RLK_ERR_UNSUPPORTED_DEVICE.  There is no CPU fallback.
+ *   - The first launch of each kernel shape on a device sets its shared-memory
+ *     size attribute and, for the clustered shapes (calls of more than 128
+ *     rows), queries how many clusters fit.  Callers that capture CUDA graphs
+ *     make one call of each size class (up to 128 rows, more) before capturing.
  */
 #ifndef RLK_H
 #define RLK_H
