@@ -96,10 +96,7 @@ int rlk_row_tile(void);
 int rlk_vocab_tile(void);
 
 /* Bytes of workspace rlk_logprob_ws needs: T * ceil(V / rlk_vocab_tile()) *
- * sizeof(rlk_partial) for the partials, plus 16 * H * 2 when T < 16 (calls with
- * fewer than 16 rows stage their hidden rows in a zero-padded 16-row copy, which
- * streams W faster; the results are bit-identical either way).  Returns 0 for
- * T <= 0, H <= 0 or V <= 0. */
+ * sizeof(rlk_partial), the partials.  Returns 0 for T <= 0, H <= 0 or V <= 0. */
 size_t rlk_logprob_workspace_size(int64_t T, int64_t H, int64_t V);
 
 /*
@@ -138,8 +135,8 @@ rlk_status rlk_logprob_ws(const void *hidden_bf16, const void *weight_bf16,
  * Writes partials[t * NVT + j] for every row t < T and tile j < NVT =
  * ceil(V / rlk_vocab_tile()); logits are never written to memory.
  *   partials  device, 16-byte aligned, partials_bytes >= T * NVT * sizeof(rlk_partial)
- * Other arguments as rlk_logprob.  (No small-T staging copy here: the partials
- * are bit-identical to those rlk_logprob computes, only possibly slower for T < 16.)
+ * Other arguments as rlk_logprob; the partials are bit-identical to those
+ * rlk_logprob computes.
  */
 rlk_status rlk_logprob_partials(const void *hidden_bf16, const void *weight_bf16,
                                 const int32_t *targets_i32, int64_t T, int64_t H, int64_t V,
@@ -177,7 +174,7 @@ rlk_status rlk_lse_merge(const rlk_partial *partials, const int32_t *targets_i32
  *   shard_begin % rlk_vocab_tile() == 0; shard_rows % rlk_vocab_tile() == 0
  *   unless the shard ends at V.  targets are global vocabulary indices.
  *   partials: [T][ceil(shard_rows / rlk_vocab_tile())] records, `a` global.
- *   Other arguments as rlk_logprob_partials (no small-T staging copy).
+ *   Other arguments as rlk_logprob_partials.
  * rlk_lse_merge_sharded: phase 2 over the shards' partials gathered as
  *   [num_shards][T][tiles_per_shard] (what an all-gather of the per-shard
  *   blocks gives); shard r holds global tiles [r * tiles_per_shard, ...), all

@@ -21,7 +21,8 @@ __all__ = ["RlkError", "lib", "logprob", "logprob_ws", "logprob_partials", "lse_
            "logprob_backward", "backward_workspace_size", "selected_token_logprob",
            "logprob_entropy", "entropy_workspace_size", "logprob_partials_shard",
            "lse_merge_sharded", "quantize_fp8_rows", "logprob_fp8", "fp8_workspace_size",
-           "quantize_fp8_weight", "unpack_fp8_weight",
+           "quantize_fp8_weight", "unpack_fp8_weight", "consistency_stats_async",
+           "stats_workspace_size", "stats_dict",
            "header_functions", "STAT_NAMES", "LIB_PATH", "HEADER_PATH"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))

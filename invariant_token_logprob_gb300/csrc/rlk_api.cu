@@ -152,18 +152,11 @@ size_t partial_bytes(int64_t T, int64_t V) {
     return size_t(T) * size_t(num_vocab_tiles(V)) * sizeof(rlk_partial);
 }
 
-// Tensor maps of h and W for the LM-head kernel.  pad_buf: NULL, or (T <
-// kMinTmaRows) room for kMinTmaRows zero-padded h rows, filled here first.
+// Tensor maps of h and W for the LM-head kernel: boxes of lmhead_a_box_rows(T)
+// h rows (zero fill past row T) and lmhead_w_box_rows(T) W rows.
 rlk_status prepare_maps(const void* h, const void* W, int64_t T, int64_t H, int64_t V,
-                        void* pad_buf, cudaStream_t stream, CUtensorMap* th, CUtensorMap* tw) {
-    int64_t h_rows = T;
-    if (pad_buf) {
-        cudaError_t e = rlk::launch_pad_rows(h, T, H, pad_buf, stream);
-        if (e != cudaSuccess) return from_cuda(e);
-        h = pad_buf;
-        h_rows = rlk::kMinTmaRows;
-    }
-    if (!encode_bf16_2d(th, h, h_rows, H, rlk::lmhead_a_box_rows(T)) ||
+                        CUtensorMap* th, CUtensorMap* tw) {
+    if (!encode_bf16_2d(th, h, T, H, rlk::lmhead_a_box_rows(T)) ||
         !encode_bf16_2d(tw, W, V, H, rlk::lmhead_w_box_rows(T)))
         return RLK_ERR_CUDA;
     return RLK_OK;
@@ -171,9 +164,9 @@ rlk_status prepare_maps(const void* h, const void* W, int64_t T, int64_t H, int6
 
 rlk_status launch_partials(const void* h, const void* W, const int32_t* tg, int64_t T,
                            int64_t H, int64_t V, float inv_temp, void* partials, int num_sms,
-                           cudaStream_t stream, void* pad_buf = nullptr) {
+                           cudaStream_t stream) {
     CUtensorMap th, tw;
-    rlk_status st = prepare_maps(h, W, T, H, V, pad_buf, stream, &th, &tw);
+    rlk_status st = prepare_maps(h, W, T, H, V, &th, &tw);
     if (st != RLK_OK) return st;
     return from_cuda(rlk::launch_lmhead_partials(&th, &tw, tg, partials, T, V, H, inv_temp,
                                                  num_sms, stream));
@@ -204,9 +197,7 @@ int rlk_vocab_tile(void) { return kVocabTile; }
 
 size_t rlk_logprob_workspace_size(int64_t T, int64_t H, int64_t V) {
     if (T <= 0 || V <= 0 || H <= 0) return 0;
-    size_t bytes = partial_bytes(T, V);
-    if (T < rlk::kMinTmaRows) bytes += size_t(rlk::kMinTmaRows) * size_t(H) * 2;
-    return bytes;
+    return partial_bytes(T, V);
 }
 
 rlk_status rlk_logprob_partials(const void* hidden_bf16, const void* weight_bf16,
@@ -257,9 +248,8 @@ rlk_status rlk_logprob_ws(const void* hidden_bf16, const void* weight_bf16,
     int dev, sms;
     if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    void* pad = T < rlk::kMinTmaRows ? static_cast<char*>(workspace) + partial_bytes(T, V) : nullptr;
     st = launch_partials(hidden_bf16, weight_bf16, targets_i32, T, H, V, inv_temp, workspace, sms,
-                         s, pad);
+                         s);
     if (st != RLK_OK) return st;
     return from_cuda(rlk::launch_lse_merge(workspace, targets_i32, T, V, out_logp_f32,
                                            out_lse_f32, out_argmax_i32, s));
@@ -302,8 +292,7 @@ rlk_status rlk_logprob(const void* hidden_bf16, const void* weight_bf16,
         }
         ws = w.ptr;
     }
-    void* pad = T < rlk::kMinTmaRows ? static_cast<char*>(ws) + partial_bytes(T, V) : nullptr;
-    st = launch_partials(hidden_bf16, weight_bf16, targets_i32, T, H, V, inv_temp, ws, sms, s, pad);
+    st = launch_partials(hidden_bf16, weight_bf16, targets_i32, T, H, V, inv_temp, ws, sms, s);
     if (st != RLK_OK) return st;
     return from_cuda(rlk::launch_lse_merge(ws, targets_i32, T, V, out_logp_f32, out_lse_f32,
                                            out_argmax_i32, s));
@@ -329,8 +318,7 @@ rlk_status rlk_logprob_partials_shard(const void* hidden_bf16, const void* weigh
     if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     CUtensorMap th, tw;
-    if ((st = prepare_maps(hidden_bf16, weight_shard_bf16, T, H, shard_rows, nullptr, s, &th,
-                           &tw)) != RLK_OK)
+    if ((st = prepare_maps(hidden_bf16, weight_shard_bf16, T, H, shard_rows, &th, &tw)) != RLK_OK)
         return st;
     return from_cuda(rlk::launch_lmhead_partials(&th, &tw, targets_i32, partials, T, shard_rows, H,
                                                  inv_temp, sms, s, shard_begin));
@@ -445,9 +433,7 @@ rlk_status rlk_logprob_fp8(const void* hidden_bf16, const uint8_t* weight_e4m3,
 
 size_t rlk_logprob_entropy_workspace_size(int64_t T, int64_t H, int64_t V) {
     if (T <= 0 || V <= 0 || H <= 0) return 0;
-    size_t bytes = partial_bytes(T, V) + (size_t(T) * size_t(num_vocab_tiles(V)) * 4 + 15) / 16 * 16;
-    if (T < rlk::kMinTmaRows) bytes += size_t(rlk::kMinTmaRows) * size_t(H) * 2;
-    return bytes;
+    return partial_bytes(T, V) + (size_t(T) * size_t(num_vocab_tiles(V)) * 4 + 15) / 16 * 16;
 }
 
 rlk_status rlk_logprob_entropy(const void* hidden_bf16, const void* weight_bf16,
@@ -470,10 +456,8 @@ rlk_status rlk_logprob_entropy(const void* hidden_bf16, const void* weight_bf16,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(workspace);
     float* ent_u = reinterpret_cast<float*>(base + partial_bytes(T, V));
-    const size_t u_bytes = (size_t(T) * size_t(num_vocab_tiles(V)) * 4 + 15) / 16 * 16;
-    void* pad = T < rlk::kMinTmaRows ? base + partial_bytes(T, V) + u_bytes : nullptr;
     CUtensorMap th, tw;
-    if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, pad, s, &th, &tw)) != RLK_OK)
+    if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, &th, &tw)) != RLK_OK)
         return st;
     cudaError_t e = rlk::launch_lmhead_entropy(&th, &tw, targets_i32, workspace, ent_u, T, V, H,
                                                inv_temp, sms, s);
@@ -485,9 +469,7 @@ rlk_status rlk_logprob_entropy(const void* hidden_bf16, const void* weight_bf16,
 
 size_t rlk_logprob_backward_workspace_size(int64_t T, int64_t H, int64_t V) {
     if (T <= 0 || V <= 0 || H <= 0) return 0;
-    size_t bytes = (size_t(T) * size_t(V) * 2 + 15) / 16 * 16;
-    if (T < rlk::kMinTmaRows) bytes += size_t(rlk::kMinTmaRows) * size_t(H) * 2;
-    return bytes;
+    return (size_t(T) * size_t(V) * 2 + 15) / 16 * 16;
 }
 
 rlk_status rlk_logprob_backward(const void* hidden_bf16, const void* weight_bf16,
@@ -510,10 +492,8 @@ rlk_status rlk_logprob_backward(const void* hidden_bf16, const void* weight_bf16
     int dev, sms;
     if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const size_t dz_bytes = (size_t(T) * size_t(V) * 2 + 15) / 16 * 16;
-    void* pad = T < rlk::kMinTmaRows ? static_cast<char*>(workspace) + dz_bytes : nullptr;
     CUtensorMap th, tw;
-    if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, pad, s, &th, &tw)) != RLK_OK)
+    if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, &th, &tw)) != RLK_OK)
         return st;
     cudaError_t e = rlk::launch_lmhead_grad_logits(&th, &tw, targets_i32, lse_f32, grad_logp_f32,
                                                    workspace, T, V, H, inv_temp, sms, s);
@@ -577,7 +557,7 @@ rlk_status rlk_selftest_wait_timeout(const void* hidden_bf16, const void* weight
     if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     CUtensorMap th, tw;
-    if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, nullptr, s, &th, &tw)) != RLK_OK)
+    if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, &th, &tw)) != RLK_OK)
         return st;
     return from_cuda(rlk::launch_lmhead_stall_selftest(&th, &tw, targets_i32, partials, T, V, H,
                                                        sms, s));

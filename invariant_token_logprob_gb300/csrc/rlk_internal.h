@@ -27,12 +27,8 @@ int lmhead_w_box_rows(int64_t T);
 // memory held and are never reported.
 int lmhead_a_box_rows(int64_t T);
 
-// Calls with fewer rows than this get their h rows copied into a zero-padded
-// buffer of this many rows before the LM-head kernel runs (see rlk_pad.cu).
+// The smallest h box the LM-head kernel copies (rows); see lmhead_a_box_rows.
 constexpr int kMinTmaRows = 16;
-
-// Copy h [T][H] (T < kMinTmaRows) into dst [kMinTmaRows][H], zeros past row T.
-cudaError_t launch_pad_rows(const void* h, int64_t T, int64_t H, void* dst, cudaStream_t stream);
 
 // Fused LM-head GEMM + vocabulary-tile epilogue.  Writes partials[T][NVT]
 // (16-byte records {m, s, a, zt}).  th / tw are 2-D tensor maps of h [T,H] and

@@ -38,9 +38,9 @@ def test_workspace_size(L):
     assert L.rlk_logprob_workspace_size(5, 0, 10) == 0
     assert L.rlk_logprob_workspace_size(4096, 4096, 151936) == 4096 * 594 * 16
     assert L.rlk_logprob_workspace_size(16, 4096, 151936) == 16 * 594 * 16
-    # fewer than 16 rows: partials plus a zero-padded 16-row copy of h
-    assert L.rlk_logprob_workspace_size(1, 4096, 151936) == 594 * 16 + 16 * 4096 * 2
-    assert L.rlk_logprob_workspace_size(3, 64, 257) == 3 * 2 * 16 + 16 * 64 * 2
+    # the partials alone, whatever T (no staging copy of h)
+    assert L.rlk_logprob_workspace_size(1, 4096, 151936) == 594 * 16
+    assert L.rlk_logprob_workspace_size(3, 64, 257) == 3 * 2 * 16
 
 
 A16 = ctypes.c_void_p(1 << 20)       # a 16-byte-aligned dummy address (never dereferenced)

@@ -256,9 +256,8 @@ def test_padding_rows_do_not_leak():
 
 @pytest.mark.parametrize("T", [1, 5, 15, 16, 17, 40])
 def test_caller_workspace_matches_cached_workspace(T):
-    """rlk_logprob_ws with an exactly-sized caller workspace (including the
-    zero-padded 16-row staging copy below 16 rows) gives rlk_logprob's bits; one
-    byte less is refused before anything runs."""
+    """rlk_logprob_ws with an exactly-sized caller workspace gives rlk_logprob's
+    bits; one byte less is refused before anything runs."""
     import invariant_token_logprob_gb300 as rlk
     d = to_dev(lm_head_inputs(T, 256, 3000, seed=50 + T))
     need = rlk.workspace_size(T, 256, 3000)
