@@ -144,6 +144,11 @@ def _need(t, dtype, name, ndim=None):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.device.type != "cuda":
         raise ValueError(f"{name} must be on a CUDA device (no CPU path exists)")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device; a tensor elsewhere would be
+        # read through a pointer that device cannot use
+        raise ValueError(f"{name} is on {t.device}, not on the current device "
+                         f"cuda:{torch.cuda.current_device()} (use torch.cuda.set_device)")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
