@@ -26,6 +26,13 @@ backward (rlk_logprob_backward on the same batch), the FP8 (W8A8) variant, the
 entropy path and the vocabulary-sharded phases (R = 2, 3, 6 shards emulated on
 one GPU).
 
+--workload picks the batch a step runs over: train4096 (the default above),
+prefill16384 (4 x 4096 = 16384 rows, H = 4096, inv_temp = fp32(1/0.7), no
+mask) or packed32768 (32768 rows, H = 5120, 1% outlier rows x8, 10% masked).
+Each prints the same JSON line (roofline, clocks, e2e, CPU baseline); the
+other regimes (decode, backward, fp8, entropy, shards) run with the default
+workload only.
+
 --impl reference times the fp64 CPU oracle (the only reference this method
 has) on the host cores, each step a bounded sample of the same workload.
 """
@@ -44,13 +51,27 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 T_CFG, H_CFG, V_CFG = 4096, 4096, 151936
+# --workload: the training-recompute batch (the default, the headline line) and
+# the two larger tensor-bound workloads, timed the same way.
+WORKLOADS = {
+    "train4096": dict(T=4096, H=4096, inv_temp=1.0, outlier_frac=0.0, mask_zero_frac=0.1,
+                      name="Qwen3-8B LM head, training recompute: T=4096 (8 packed x 512), "
+                           "H=4096, V=151936"),
+    "prefill16384": dict(T=16384, H=4096, inv_temp=float(__import__("numpy").float32(1 / 0.7)),
+                         outlier_frac=0.0, mask_zero_frac=0.0,
+                         name="prefill vs decode phase consistency: 4 sequences x 4096 = "
+                              "T=16384, H=4096, V=151936, inv_temp=fp32(1/0.7)"),
+    "packed32768": dict(T=32768, H=5120, inv_temp=1.0, outlier_frac=0.01, mask_zero_frac=0.1,
+                        name="large packed batch: T=32768, H=5120, V=151936, 1% outlier rows "
+                             "x8, 10% of tokens masked out of the statistics"),
+}
 METRIC = "tokens/s of batch-invariant logprob (H=4096,V=151936); % of TC/HBM roofline"
-WORKLOAD = "Qwen3-8B LM head, training recompute: T=4096 (8 packed x 512), H=4096, V=151936"
 KERNEL_SOURCES = ["invariant_token_logprob_gb300/csrc/rlk_lmhead.cu",
                   "invariant_token_logprob_gb300/csrc/rlk_sm103.cuh",
                   "invariant_token_logprob_gb300/csrc/rlk_lse.cuh",
                   "invariant_token_logprob_gb300/csrc/rlk_internal.h"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lmhead_partials_T4096_H4096_V151936.md")
+def traffic_file(T, H, V):
+    return os.path.join(ROOT, "profiles", f"lmhead_partials_T{T}_H{H}_V{V}.md")
 
 
 def parse():
@@ -59,6 +80,10 @@ def parse():
     p.add_argument("--steps", type=int, default=300)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="train4096", choices=sorted(WORKLOADS),
+                   help="train4096 (default): T=4096, H=4096; prefill16384: T=16384, "
+                        "inv_temp=fp32(1/0.7); packed32768: T=32768, H=5120 (the other regimes "
+                        "-- decode, backward, fp8, entropy, shards -- run with the default only)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-backward", action="store_true")
@@ -95,18 +120,19 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch of the LM-head kernel from the committed ncu summary,
-    if that capture was taken of the kernel sources as they are now."""
-    if not os.path.exists(TRAFFIC_FILE):
+def recorded_traffic(T, H, V):
+    """DRAM bytes per launch of the LM-head kernel from the committed ncu summary
+    of this workload, if that capture was taken of the kernel sources as they are
+    now."""
+    path = traffic_file(T, H, V)
+    if not os.path.exists(path):
         return None
-    import re
-    text = open(TRAFFIC_FILE).read()
+    text = open(path).read()
     mh = re.search(r"^kernel_hash:\s*([0-9a-f]+)\s*$", text, re.M)
     mt = re.search(r"^traffic_bytes_per_launch:\s*([0-9]+)\s*$", text, re.M)
     if not mh or not mt or mh.group(1) != kernel_hash():
         return None
-    return dict(bytes_per_launch=int(mt.group(1)), source=os.path.relpath(TRAFFIC_FILE, ROOT))
+    return dict(bytes_per_launch=int(mt.group(1)), source=os.path.relpath(path, ROOT))
 
 
 class ClockSampler:
@@ -209,7 +235,7 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
-def cpu_oracle_sample(d, rows_per_thread=8):
+def cpu_oracle_sample(d, wl, rows_per_thread=8):
     """Time the oracle as it stands on a bounded sample of rows of the workload."""
     import numpy as np
     import oracle
@@ -222,11 +248,11 @@ def cpu_oracle_sample(d, rows_per_thread=8):
     W = d["W"].cpu()
     tg = d["targets"].cpu()
     t0 = time.perf_counter()
-    oracle.logprob(h, W, tg, 1.0, rows=rows, lib=lib)
+    oracle.logprob(h, W, tg, wl["inv_temp"], rows=rows, lib=lib)
     dt = time.perf_counter() - t0
     return dict(value=len(rows) / dt, unit="tokens/s", cores=threads, kind="oracle",
-                sample=f"{len(rows)} seeded rows of the T=4096 batch (full V=151936, H=4096), "
-                       f"fp64 oracle, OpenMP over rows, {dt:.1f} s")
+                sample=f"{len(rows)} seeded rows of the T={wl['T']} batch (full V={V_CFG}, "
+                       f"H={wl['H']}), fp64 oracle, OpenMP over rows, {dt:.1f} s")
 
 
 def run_reference(args):
@@ -239,16 +265,18 @@ def run_reference(args):
     lib = oracle.load()
     threads = oracle.num_threads(lib)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    d = lm_head_inputs(T_CFG, H_CFG, V_CFG, seed=1000, device=dev, hidden="rms", mask_zero_frac=0.1)
+    wl = WORKLOADS[args.workload]
+    d = lm_head_inputs(wl["T"], wl["H"], V_CFG, seed=1000, device=dev, hidden="rms",
+                       outlier_frac=wl["outlier_frac"], mask_zero_frac=wl["mask_zero_frac"])
     h, W, tg = d["h"].cpu(), d["W"].cpu(), d["targets"].cpu()
     rows_per_step = threads  # one row per core per step: about a second a step
     import numpy as np
     g = np.random.default_rng(7)
     times = []
     for i in range(args.warmup + args.steps):
-        rows = np.sort(g.choice(T_CFG, size=rows_per_step, replace=False))
+        rows = np.sort(g.choice(wl["T"], size=rows_per_step, replace=False))
         t0 = time.perf_counter()
-        oracle.logprob(h, W, tg, 1.0, rows=rows, lib=lib)
+        oracle.logprob(h, W, tg, wl["inv_temp"], rows=rows, lib=lib)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -258,7 +286,8 @@ def run_reference(args):
                 steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * total / len(times),
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
                 data="synthetic",
-                config=dict(workload=WORKLOAD, T=T_CFG, H=H_CFG, V=V_CFG, inv_temp=1.0,
+                config=dict(workload=wl["name"], T=wl["T"], H=wl["H"], V=V_CFG,
+                            inv_temp=wl["inv_temp"],
                             step=f"oracle over {rows_per_step} seeded rows of the batch"),
                 cpu_baseline=dict(value=value, unit="tokens/s", cores=threads, kind="oracle",
                                   sample=f"{rows_per_step} rows per step, full V and H"),
@@ -529,16 +558,19 @@ def run_ours(args):
     pk = peaks()
 
     # ---------------------------------------------------------------- inputs
-    d = lm_head_inputs(T_CFG, H_CFG, V_CFG, seed=1000 + rank, device=dev, hidden="rms",
-                       mask_zero_frac=0.1)
+    wl = WORKLOADS[args.workload]
+    default_wl = args.workload == "train4096"
+    d = lm_head_inputs(wl["T"], wl["H"], V_CFG, seed=1000 + rank, device=dev, hidden="rms",
+                       outlier_frac=wl["outlier_frac"], mask_zero_frac=wl["mask_zero_frac"])
     h, W, tg, mask = d["h"], d["W"], d["targets"], d["mask"]
-    T, H, V = T_CFG, H_CFG, V_CFG
+    T, H, V = wl["T"], wl["H"], V_CFG
+    it = wl["inv_temp"]
     nvt = (V + rlk.vocab_tile() - 1) // rlk.vocab_tile()
     partials = torch.empty((T, nvt, 4), dtype=torch.float32, device=dev)
     out = [torch.empty(T, device=dev, dtype=dt) for dt in (torch.float32, torch.float32, torch.int32)]
     stream = torch.cuda.current_stream(dev)
     # the "rollout" logprobs the acceptance statistics compare against
-    rollout = rlk.logprob(h, W, tg, 1.0)[0].clone()
+    rollout = rlk.logprob(h, W, tg, it)[0].clone()
 
     # each step's 8 statistics land in its own row, stream-ordered (no host sync
     # inside the loop); they are read and checked once the timed region is over
@@ -548,7 +580,7 @@ def run_ours(args):
     def step(i, ev=None):
         if ev is not None:
             ev[0].record(stream)
-        rlk.logprob_partials(h, W, tg, 1.0, out=partials)
+        rlk.logprob_partials(h, W, tg, it, out=partials)
         if ev is not None:
             ev[1].record(stream)
         rlk.lse_merge(partials, tg, V, out=out)
@@ -621,7 +653,7 @@ def run_ours(args):
     def compute_and_d2h(b):
         stream.wait_event(h2d_done[b])
         stream.wait_event(d2h_done[b])  # its previous results have left the device
-        lp, lse, am = rlk.logprob(h_dev[b], W, tg_dev[b], 1.0, out=outs_dev[b])
+        lp, lse, am = rlk.logprob(h_dev[b], W, tg_dev[b], it, out=outs_dev[b])
         rlk.consistency_stats_async(lp, rollout, mask, out=st_dev[b], workspace=stats_ws)
         computed[b].record(stream)
         with torch.cuda.stream(copy_stream):
@@ -664,24 +696,25 @@ def run_ours(args):
                         "read on the host during step i+1")
 
     # ---------------------------------------------------------------- regimes
+    # the other regimes are measured on the default workload's batch only
     decode = None
-    if not args.no_decode:
+    if not args.no_decode and default_wl:
         decode = decode_points(rlk, torch, W, stream, pk)
     backward = None
-    if not args.no_backward:
+    if not args.no_backward and default_wl:
         backward = backward_point(rlk, torch, h, W, tg, pk)
     fp8 = None
-    if not args.no_fp8:
+    if not args.no_fp8 and default_wl:
         fp8 = fp8_points(rlk, torch, h, W, tg, pk)
-    entropy = None if args.no_entropy else entropy_point(rlk, torch, h, W, tg, pk)
-    sharded = None if args.no_shard else shard_points(rlk, torch, h, W, tg, pk)
+    entropy = None if (args.no_entropy or not default_wl) else entropy_point(rlk, torch, h, W, tg, pk)
+    sharded = None if (args.no_shard or not default_wl) else shard_points(rlk, torch, h, W, tg, pk)
 
     if rank != 0:
         return 0
 
     flops = 2.0 * T * H * V
     achieved = flops / gemm_avg / 1e12
-    tr = recorded_traffic()
+    tr = recorded_traffic(T, H, V)
     roofline = dict(bound="tensor", achieved=achieved, peak=pk["bf16_tflops"], unit="TFLOP/s",
                     frac=achieved / pk["bf16_tflops"],
                     frac_of_sustained=achieved / pk["bf16_tflops_sustained"],
@@ -693,13 +726,14 @@ def run_ours(args):
                     step_share=gemm_avg * args.steps / (elapsed if world == 1 else elapsed))
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_oracle_sample(d)
+        cpu = cpu_oracle_sample(d, wl)
     clk = clocks.summary()
     line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=1e3 * elapsed / args.steps,
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
                 data="synthetic",
-                config=dict(workload=WORKLOAD, T=T, H=H, V=V, inv_temp=1.0, masked_frac=0.1,
+                config=dict(workload=wl["name"], T=T, H=H, V=V, inv_temp=it,
+                            masked_frac=wl["mask_zero_frac"], outlier_frac=wl["outlier_frac"],
                             l2="inputs larger than L2 (W 1.245 GB vs 129 MB L2): no flush",
                             step="partials (fused GEMM+epilogue) -> merge -> consistency stats",
                             parallelism=f"dp{world} (rows; no collective)"),

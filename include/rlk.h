@@ -68,7 +68,9 @@ typedef enum rlk_status {
     RLK_ERR_UNSUPPORTED_DEVICE = 3, /* no CUDA device, or not compute capability 10.3 */
     RLK_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed              */
     RLK_ERR_WORKSPACE = 5,          /* workspace too small / could not be obtained    */
-    RLK_ERR_TIMEOUT = 6             /* a device-side bounded wait ran out (reported by
+    RLK_ERR_TIMEOUT = 6,            /* a device-side bounded wait ran out (reported by
+                                       rlk_check_device_error)                       */
+    RLK_ERR_TARGET_RANGE = 7        /* a merge saw a target >= V (reported by
                                        rlk_check_device_error)                       */
 } rlk_status;
 
@@ -103,8 +105,12 @@ size_t rlk_logprob_workspace_size(int64_t T, int64_t H, int64_t V);
  * Selected-token logprob, LSE and argmax for T rows.
  *   hidden_bf16   device, [T][H] bf16, 16-byte aligned
  *   weight_bf16   device, [V][H] bf16, 16-byte aligned
- *   targets_i32   device, [T]; a target outside [0, V) marks an ignored row:
- *                 its logp is written as 0.0f (lse and argmax are still written)
+ *   targets_i32   device, [T]; a negative target marks an ignored row: its logp
+ *                 is written as 0.0f (lse and argmax are still written).  A
+ *                 target >= V cannot be checked on the host without reading
+ *                 device memory; the row is treated like an ignored one and
+ *                 also counted in a per-device word, which the next
+ *                 rlk_check_device_error reports as RLK_ERR_TARGET_RANGE.
  *   T >= 0 (T == 0: returns RLK_OK, launches nothing), 1 <= H, H % 8 == 0,
  *   1 <= V <= 2^31 - 1, T * ceil(V / vocab_tile) representable in int64
  *   inv_temp      finite and > 0; z = fp32 accumulator * inv_temp (one multiply)
@@ -328,22 +334,26 @@ rlk_status rlk_consistency_stats_async(const float *logp_a, const float *logp_b,
 /*
  * rlk_logprob for callers that cannot allocate device memory.  The pages
  * describe no counterpart of this entry point; it exists for this library's
- * users.  Callers that cannot allocate include code running under CUDA-graph
- * capture, engines whose device memory is pre-reserved by their own allocator,
- * and decode loops that must never block on an allocation; they may also have
- * no spare buffer to pass to rlk_logprob_ws.
+ * users.  Callers that cannot allocate include inference engines whose device
+ * memory is pre-reserved by their own allocator (a stray cudaMalloc can fail
+ * or fragment that pool) and decode loops that must never block on an
+ * allocation; they may also have no spare buffer to pass to rlk_logprob_ws.
  *
  * Same arguments, results and bits as rlk_logprob (inputs and outputs are still
  * the caller's).  Instead of a workspace, the partials live in one fixed device
- * array of RLK_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
- * loads the library keeps for the life of the process.
+ * array of RLK_NOALLOC_SCRATCH_BYTES inside the library, reserved on each
+ * device where the library's device code is loaded (every visible device under
+ * eager module loading; under lazy loading, the devices it has run on) for the
+ * life of the process.
  *   Limit: rlk_logprob_workspace_size(T, H, V) <= RLK_NOALLOC_SCRATCH_BYTES, i.e.
  *   up to 1765 rows per call at V = 151936; larger problems return
  *   RLK_ERR_WORKSPACE before anything is launched (split the rows into calls).
  *   Allocates nothing: no cudaMalloc / cudaFree or allocating library routine.
- *   Set-up: the first call on each device looks up the array's device address
+ *   Set-up: the first call on each device checks it (RLK_ERR_UNSUPPORTED_DEVICE
+ *   unless compute capability 10.3) and looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is kept for the life of the
+ *   process, so do not use this entry point across a cudaDeviceReset.
  *   Sharing: every call on a device uses the same array and leaves its
  *   contents behind (nothing in it needs to start at zero).  Calls whose
  *   execution overlaps on the GPU -- on different streams, or from different
@@ -357,14 +367,29 @@ rlk_status rlk_logprob_noalloc(const void *hidden_bf16, const void *weight_bf16,
                                int32_t *out_argmax_i32, rlk_stream_t stream);
 
 /*
- * Every device-side wait in the library's kernels is bounded in time.  If one
- * runs out, the kernel records it in a per-device error word, drains its own
- * in-flight copies, releases its tensor memory and returns (its outputs are
- * then unspecified).  This call synchronises `stream`, reads and clears the
- * word of the current device and returns RLK_ERR_TIMEOUT if it was set,
- * RLK_ERR_CUDA if the stream reported an error, else RLK_OK.
+ * Device-side error records, one set per device, kept by the kernels because
+ * they cannot be detected on the host before a launch:
+ *   - Every device-side wait in the library's kernels is bounded in time.  If
+ *     one runs out, the kernel records it in a per-device error word, drains
+ *     its own in-flight copies, releases its tensor memory and returns (its
+ *     outputs are then unspecified).
+ *   - Every merge (rlk_logprob and all entry points that end in a merge) counts
+ *     the rows whose target was >= V; those rows got logp = 0.0f, as ignored
+ *     rows do.  (The backward treats such rows as ignored without counting
+ *     them: it runs after a forward call on the same targets, which did.)
+ * rlk_check_device_error synchronises `stream`, reads and clears the current
+ * device's records and returns RLK_ERR_TIMEOUT if a wait ran out, else
+ * RLK_ERR_TARGET_RANGE if a target >= V was seen, RLK_ERR_CUDA if the stream
+ * reported an error, else RLK_OK.
+ * rlk_take_device_errors does the same read and clear and returns the records
+ * themselves (either pointer may be NULL): *wait_error_bits bit 0 = a wait
+ * ran out, bit 1 = a teardown wait ran out; *target_range_rows = the number of
+ * rows with a target >= V since the last read.  Returns RLK_OK unless the
+ * stream or the read failed.
  */
 rlk_status rlk_check_device_error(rlk_stream_t stream);
+rlk_status rlk_take_device_errors(rlk_stream_t stream, uint32_t *wait_error_bits,
+                                  uint64_t *target_range_rows);
 
 /*
  * Self-test of the failure detection above, for test suites: launches the

@@ -17,7 +17,7 @@ import re
 from typing import Optional
 
 __all__ = ["RlkError", "lib", "logprob", "logprob_ws", "logprob_partials", "lse_merge",
-           "consistency_stats", "workspace_size", "check_device_error", "vocab_tile", "row_tile",
+           "consistency_stats", "workspace_size", "check_device_error", "take_device_errors", "vocab_tile", "row_tile",
            "logprob_backward", "backward_workspace_size", "selected_token_logprob",
            "logprob_entropy", "entropy_workspace_size", "logprob_partials_shard",
            "lse_merge_sharded", "quantize_fp8_rows", "logprob_fp8", "fp8_workspace_size",
@@ -34,7 +34,7 @@ STAT_NAMES = ("max_abs", "mean_abs", "std_abs", "k3_mean", "sum_delta", "n_valid
 
 _STATUS = {0: "RLK_OK", 1: "RLK_ERR_INVALID_ARG", 2: "RLK_ERR_ALIGNMENT",
            3: "RLK_ERR_UNSUPPORTED_DEVICE", 4: "RLK_ERR_CUDA", 5: "RLK_ERR_WORKSPACE",
-           6: "RLK_ERR_TIMEOUT"}
+           6: "RLK_ERR_TIMEOUT", 7: "RLK_ERR_TARGET_RANGE"}
 
 
 class RlkError(RuntimeError):
@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.rlk_selftest_wait_timeout.argtypes = [P, P, P, P, P]
         L.rlk_check_device_error.restype = st
         L.rlk_check_device_error.argtypes = [P]
+        L.rlk_take_device_errors.restype = st
+        L.rlk_take_device_errors.argtypes = [P, P, P]
         L.rlk_shutdown.restype = st
         L.rlk_shutdown.argtypes = []
         L.rlk_logprob_partials_shard.restype = st
@@ -306,8 +308,19 @@ def stats_dict(out):
 
 
 def check_device_error(stream=None):
-    """Raise RlkError(RLK_ERR_TIMEOUT) if a device-side bounded wait ran out."""
+    """Raise RlkError(RLK_ERR_TIMEOUT) if a device-side bounded wait ran out, or
+    RlkError(RLK_ERR_TARGET_RANGE) if a merge saw a target >= V (synchronises)."""
     _check(lib().rlk_check_device_error(_stream(stream)), "rlk_check_device_error")
+
+
+def take_device_errors(stream=None):
+    """rlk_take_device_errors: read and clear the device's error records; returns
+    (wait_error_bits, target_range_rows) (synchronises)."""
+    bits = ctypes.c_uint32(0)
+    rows = ctypes.c_uint64(0)
+    _check(lib().rlk_take_device_errors(_stream(stream), ctypes.byref(bits), ctypes.byref(rows)),
+           "rlk_take_device_errors")
+    return int(bits.value), int(rows.value)
 
 
 def backward_workspace_size(T: int, H: int, V: int) -> int:

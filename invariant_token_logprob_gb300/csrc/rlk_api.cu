@@ -188,6 +188,8 @@ const char* rlk_status_string(int status) {
         case RLK_ERR_CUDA: return "RLK_ERR_CUDA: a CUDA call failed";
         case RLK_ERR_WORKSPACE: return "RLK_ERR_WORKSPACE: workspace too small or unavailable";
         case RLK_ERR_TIMEOUT: return "RLK_ERR_TIMEOUT: a device-side bounded wait ran out";
+        case RLK_ERR_TARGET_RANGE:
+            return "RLK_ERR_TARGET_RANGE: a row's target was >= V (its logp was written as 0)";
         default: return "unknown rlk_status";
     }
 }
@@ -563,15 +565,29 @@ rlk_status rlk_selftest_wait_timeout(const void* hidden_bf16, const void* weight
                                                        sms, s));
 }
 
-rlk_status rlk_check_device_error(rlk_stream_t stream) {
+rlk_status rlk_take_device_errors(rlk_stream_t stream, uint32_t* wait_error_bits,
+                                  uint64_t* target_range_rows) {
     int dev, sms;
     rlk_status st = current_device(&dev, &sms);
     if (st != RLK_OK) return st;
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return RLK_ERR_CUDA;
     unsigned int word = 0;
+    unsigned long long rows = 0;
     if (rlk::lmhead_take_error(&word) != cudaSuccess) return RLK_ERR_CUDA;
-    return word ? RLK_ERR_TIMEOUT : RLK_OK;
+    if (rlk::take_target_range_rows(&rows) != cudaSuccess) return RLK_ERR_CUDA;
+    if (wait_error_bits) *wait_error_bits = word;
+    if (target_range_rows) *target_range_rows = rows;
+    return RLK_OK;
+}
+
+rlk_status rlk_check_device_error(rlk_stream_t stream) {
+    uint32_t word = 0;
+    uint64_t rows = 0;
+    rlk_status st = rlk_take_device_errors(stream, &word, &rows);
+    if (st != RLK_OK) return st;
+    if (word) return RLK_ERR_TIMEOUT;
+    return rows ? RLK_ERR_TARGET_RANGE : RLK_OK;
 }
 
 rlk_status rlk_shutdown(void) {

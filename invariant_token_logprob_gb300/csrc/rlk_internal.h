@@ -98,6 +98,11 @@ cudaError_t launch_lmhead_stall_selftest(const CUtensorMap* th, const CUtensorMa
 // bounded wait ran out).  Synchronous on the current device.
 cudaError_t lmhead_take_error(unsigned int* out);
 
+// Reads and clears the per-device count of rows whose target was >= V, kept by
+// every merge kernel (such rows get logp = 0 like ignored rows).  Synchronous on
+// the current device.
+cudaError_t take_target_range_rows(unsigned long long* out);
+
 // Forward records plus the per-tile entropy statistic ent_u [T][NVT]
 // (sum exp(z - m)(z - m) about the tile's max m).
 cudaError_t launch_lmhead_entropy(const CUtensorMap* th, const CUtensorMap* tw,

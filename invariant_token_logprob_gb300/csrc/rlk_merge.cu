@@ -10,9 +10,12 @@
 // The tree depends only on NVT = ceil(V / 256), never on T, and lse_combine is
 // commutative bit for bit, so all lanes finish with identical bits.
 //   lse = M + log(S),  argmax = A,  logp = zt(tile of target) - lse
-// (logp = 0 for a target outside [0, V)).  The entropy variant also folds
-// u = sum exp(z - m)(z - m) per tile and writes entropy = log S - U / S, the
-// softmax entropy -sum p log p over the whole vocabulary.
+// (logp = 0 for a target outside [0, V); a target >= V is also counted in a
+// per-device word that rlk_check_device_error reports: unlike a negative
+// target it is no "ignore" marker but an out-of-range index).  The entropy
+// variant also folds u = sum exp(z - m)(z - m) per tile and writes
+// entropy = log S - U / S, the softmax entropy -sum p log p over the whole
+// vocabulary.
 #include <limits.h>
 
 #include "rlk_internal.h"
@@ -23,6 +26,14 @@ namespace rlk {
 namespace {
 
 constexpr int kMergeWarps = 8;
+
+}  // namespace
+
+// Rows whose target was >= V, counted by every merge on this device since the
+// last read (take_target_range_rows).
+__device__ unsigned long long g_target_range_rows;
+
+namespace {
 
 // Record of global tile j for `row`: [T][nvt] unsharded, or [R][T][nvt_shard]
 // when the partials were gathered from vocabulary shards.
@@ -99,6 +110,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
         if (tgt >= 0 && tgt < V)
             logp = __ldg(record<kSharded>(partials, row, T, nvt, nvt_shard, tgt / kVocabTile)).w -
                    lse;
+        else if (tgt >= V)
+            atomicAdd(&g_target_range_rows, 1ull);
         out_logp[row] = logp;
         out_lse[row] = lse;
         out_argmax[row] = a;
@@ -158,6 +171,15 @@ cudaError_t launch_lse_merge_entropy(const void* partials, const float* ent_u,
     return launch_merge<true, false>(T, stream, static_cast<const float4*>(partials), targets,
                                      int(V), nvt, out_logp, out_lse, out_argmax, ent_u, out_entropy,
                                      0);
+}
+
+cudaError_t take_target_range_rows(unsigned long long* out) {
+    unsigned long long v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_target_range_rows, sizeof v);
+    if (e != cudaSuccess) return e;
+    if (v) e = cudaMemcpyToSymbol(g_target_range_rows, &zero, sizeof zero);
+    *out = v;
+    return e;
 }
 
 }  // namespace rlk

@@ -1,23 +1,25 @@
 // rlk_noalloc.cu -- rlk_logprob_noalloc: the selected-token logprob for
 // callers that are not allowed to allocate device memory.
 //
-// Who needs it: code that runs while a CUDA graph is being captured (an
-// allocation there is either illegal or becomes part of the graph), inference
-// engines whose device memory is reserved up front by their own allocator (a
-// stray cudaMalloc can fail outright or fragment the reserved pool), and
-// latency-critical decode loops that must never block on the allocator.  Such
-// callers cannot use rlk_logprob (it grows a cached workspace) and may have no
-// buffer to hand to rlk_logprob_ws.
+// Who needs it: inference engines whose device memory is reserved up front by
+// their own allocator (a stray cudaMalloc can fail outright or fragment the
+// reserved pool), and latency-critical decode loops that must never block on
+// the allocator.  Such callers cannot use rlk_logprob (it grows a cached
+// workspace) and may have no buffer to hand to rlk_logprob_ws.
 //
 // How: the per-(row, vocabulary tile) partials that the two kernels exchange
 // live in one fixed array in this file's device memory, RLK_NOALLOC_SCRATCH_BYTES
-// large, which every GPU that loads the library holds until the process exits.
-// Host code cannot use the array's name as a device address (on the host it
-// only names a stand-in object), so the first call on each device looks up the
-// array's real device address with cudaGetSymbolAddress while that device is
-// current, and every call passes that address to the unchanged logprob path
-// (rlk_logprob_ws).  Nothing is allocated or freed, by this file or by the
-// path it calls.
+// large, reserved on every device where the library's device code is loaded
+// (with lazy module loading, the devices the library has launched on) until the
+// process exits.  Host code cannot use the array's name as a device address (on
+// the host it only names a stand-in object), so the first call on each device
+// checks the device, then looks up the array's real device address with
+// cudaGetSymbolAddress while that device is current, and every call passes that
+// address to the unchanged logprob path (rlk_logprob_ws).  Nothing is allocated
+// or freed, by this file or by the path it calls.  The address is cached per
+// device for the life of the process: after a cudaDeviceReset the module is
+// loaded afresh and the array may move, so this entry point must not be used
+// across a device reset.
 #include <cuda_runtime.h>
 #include <limits.h>
 #include <stdint.h>
@@ -61,7 +63,19 @@ extern "C" rlk_status rlk_logprob_noalloc(const void* hidden_bf16, const void* w
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!g_scratch_ptr[dev]) {
-            // One-time set-up for this (current) device.
+            // One-time set-up for this (current) device.  The library holds
+            // device code for compute capability 10.3 only: on any other device
+            // the array does not exist, so refuse it first, with the status the
+            // other entry points give.
+            int major = 0, minor = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
+                    cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+                    cudaSuccess) {
+                cudaGetLastError();
+                return RLK_ERR_UNSUPPORTED_DEVICE;
+            }
+            if (major != 10 || minor != 3) return RLK_ERR_UNSUPPORTED_DEVICE;
             void* p = nullptr;
             cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
             if (e != cudaSuccess || p == nullptr) {

@@ -51,3 +51,28 @@ def assert_bitwise(a, b, what=""):
         bx, by = bits(x), bits(y)
         n = int(np.count_nonzero(bx != by))
         assert n == 0, f"{what}: {n} bitwise mismatches in {name}"
+
+
+def assert_block_records(P, bs, h, W, bn, inv_temp=1.0, j0=0, what=""):
+    """Per-(row, vocabulary tile) records {m, s, a, zt} of the CUDA path, P
+    [T, ntiles, 4] float32 for global tiles j0 .. j0 + ntiles - 1, against the
+    oracle's per-block statistics bs (oracle.block_stats over the whole V).
+    m, s, zt within 1e-5 relative; a exact wherever the tile's largest logit is
+    clear of its runner-up by more than 1e-3 (h, W: bf16 CPU tensors, used only
+    to find those tiles)."""
+    m, s = P[..., 0].astype(np.float64), P[..., 1].astype(np.float64)
+    a, zt = P[..., 2].view(np.int32), P[..., 3].astype(np.float64)
+    nt = m.shape[1]
+    sl = slice(j0, j0 + nt)
+    bm, bsum, bzt, ba = bs["m"][:, sl], bs["s"][:, sl], bs["zt"][:, sl], bs["a"][:, sl]
+    assert m.shape == bm.shape, (what, m.shape, bm.shape)
+    assert np.all(np.abs(m - bm) <= 1e-5 * np.maximum(1, np.abs(bm))), f"{what}: m"
+    assert np.all(np.abs(s - bsum) <= 1e-5 * bsum), f"{what}: s"
+    assert np.all(np.abs(zt - bzt) <= 1e-5 * np.maximum(1, np.abs(bzt))), f"{what}: zt"
+    V = W.shape[0]
+    z = (h.double() @ W.double().T).numpy() * float(np.float32(inv_temp))
+    for j in range(nt):
+        g = j0 + j
+        zz = np.sort(z[:, g * bn:min(V, (g + 1) * bn)], axis=1)
+        clear = (zz[:, -1] - zz[:, -2] > 1e-3) if zz.shape[1] > 1 else np.ones(z.shape[0], bool)
+        assert np.array_equal(a[clear, j], ba[clear, j]), f"{what}: a of tile {g}"

@@ -27,7 +27,7 @@ def test_abi_version_and_tiles(L):
     assert L.rlk_abi_version() == 1
     assert L.rlk_row_tile() == 128
     assert L.rlk_vocab_tile() == 256
-    for s in range(7):
+    for s in range(8):
         assert L.rlk_status_string(s).decode().startswith("RLK_")
     assert L.rlk_status_string(99) == b"unknown rlk_status"
 
@@ -120,6 +120,12 @@ def test_valid_call_without_gpu_reports_device_error(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; covered by the gpu tests")
     assert _lp(L) == 3  # RLK_ERR_UNSUPPORTED_DEVICE
+    f = ctypes.c_float(1.0)
+    assert L.rlk_logprob_noalloc(A16, A16, A16, 4, 64, 100, f, A16, A16, A16, None) == 3
+    assert L.rlk_check_device_error(None) == 3
+    bits, rows = ctypes.c_uint32(5), ctypes.c_uint64(5)
+    assert L.rlk_take_device_errors(None, ctypes.byref(bits), ctypes.byref(rows)) == 3
+    assert (bits.value, rows.value) == (5, 5)  # left untouched
 
 
 def test_binding_refuses_cpu_tensors():

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import assert_bitwise, assert_parity, gpu_logprob, to_dev
+from gpu_util import assert_bitwise, assert_block_records, assert_parity, gpu_logprob, to_dev
 from invariant_token_logprob_gb300.inputs import lm_head_inputs, tiny_inputs
 
 pytestmark = pytest.mark.gpu
@@ -82,12 +82,40 @@ def test_exact_integer_logits_and_ties(olib):
 
 def test_ignored_targets_write_zero(olib):
     d = lm_head_inputs(16, 64, 600, seed=9)
-    d["targets"][:4] = torch.tensor([-1, 600, -100, 2**31 - 1], dtype=torch.int32)
+    d["targets"][:2] = torch.tensor([-1, -100], dtype=torch.int32)
     dd = to_dev(d)
-    gpu = gpu_logprob(dd["h"], dd["W"], dd["targets"])
-    assert np.all(gpu[0][:4] == 0.0)
+    gpu = gpu_logprob(dd["h"], dd["W"], dd["targets"])  # negative: ignored, nothing flagged
+    assert np.all(gpu[0][:2] == 0.0)
     ref = oracle.logprob(d["h"], d["W"], d["targets"], lib=olib)
     assert_parity(gpu, ref, what="ignored targets")
+
+
+@pytest.mark.parametrize("T", [5, 300])  # single CTA and CTA pair shapes
+def test_targets_beyond_V_are_flagged(olib, T):
+    """A target >= V cannot be checked on the host: the row gets logp = 0 like an
+    ignored row, and the merge counts it in the device's error records, which
+    rlk_check_device_error reports as RLK_ERR_TARGET_RANGE (then cleared)."""
+    import invariant_token_logprob_gb300 as rlk
+    V = 600
+    d = lm_head_inputs(T, 64, V, seed=9)
+    d["targets"][:4] = torch.tensor([-1, V, V + 7, 2**31 - 1], dtype=torch.int32)
+    dd = to_dev(d)
+    rlk.check_device_error()
+    lp, lse, am = rlk.logprob(dd["h"], dd["W"], dd["targets"])
+    bits, rows = rlk.take_device_errors()
+    assert (bits, rows) == (0, 3)
+    gpu = (lp.cpu().numpy(), lse.cpu().numpy(), am.cpu().numpy())
+    assert np.all(gpu[0][:4] == 0.0)
+    assert_parity(gpu, oracle.logprob(d["h"], d["W"], d["targets"], lib=olib), what="targets >= V")
+    rlk.logprob(dd["h"], dd["W"], dd["targets"])
+    with pytest.raises(rlk.RlkError) as e:
+        rlk.check_device_error()
+    assert e.value.status == 7  # RLK_ERR_TARGET_RANGE
+    rlk.check_device_error()  # cleared by the read
+    # in-range targets raise nothing
+    dd["targets"][:4] = torch.tensor([0, V - 1, 1, 2], dtype=torch.int32, device="cuda")
+    rlk.logprob(dd["h"], dd["W"], dd["targets"])
+    assert rlk.take_device_errors() == (0, 0)
 
 
 def test_temperature_is_one_exact_multiply():
@@ -109,19 +137,7 @@ def test_partials_match_oracle_block_stats(olib):
     rlk.check_device_error()
     P = P.cpu().numpy()
     bs = oracle.block_stats(d["h"], d["W"], d["targets"], rlk.vocab_tile(), 1.0, lib=olib)
-    m, s = P[..., 0].astype(np.float64), P[..., 1].astype(np.float64)
-    a, zt = P[..., 2].view(np.int32), P[..., 3].astype(np.float64)
-    assert m.shape == bs["m"].shape
-    assert np.all(np.abs(m - bs["m"]) <= 1e-5 * np.maximum(1, np.abs(bs["m"])))
-    assert np.all(np.abs(s - bs["s"]) <= 1e-5 * bs["s"])
-    assert np.all(np.abs(zt - bs["zt"]) <= 1e-5 * np.maximum(1, np.abs(bs["zt"])))
-    # argmax exact wherever the block's max is clear of the runner-up in the oracle
-    z = (d["h"].double() @ d["W"].double().T).numpy()
-    nb = m.shape[1]
-    for j in range(nb):
-        zz = np.sort(z[:, j * 256:min(V, (j + 1) * 256)], axis=1)
-        clear = (zz[:, -1] - zz[:, -2] > 1e-3) if zz.shape[1] > 1 else np.ones(T, bool)
-        assert np.array_equal(a[clear, j], bs["a"][clear, j])
+    assert_block_records(P, bs, d["h"], d["W"], rlk.vocab_tile(), what="partials")
 
 
 def test_merge_alone_matches_oracle_fp64_merge(olib):

@@ -1,6 +1,6 @@
 """rlk_logprob_noalloc: the allocation-free entry point for callers that cannot
-allocate device memory (graph capture, engines with a pre-reserved memory
-pool, decode loops that must not block on the allocator).
+allocate device memory (engines with a pre-reserved memory pool, decode loops
+that must not block on the allocator).
 
 Called through the C ABI with ctypes, twice in a row with different inputs, and
 compared with rlk_logprob (the existing entry point) under the parity
