@@ -275,18 +275,25 @@ rlk_status rlk_logprob_entropy(const void *hidden_bf16, const void *weight_bf16,
  *                                          when accumulate_grad_weight != 0)
  * The logits are recomputed on the forward's fixed tiles (same main loop, so
  * the same fp32 logits), p uses the forward's lse, dz is rounded once to bf16
- * and the two products run as bf16 x bf16 -> fp32 library GEMMs.
+ * and the two products run as bf16 x bf16 -> fp32 tensor-core GEMMs of this
+ * library (tcgen05, CTA pairs), each output element one accumulator summed in
+ * a fixed k order.  grad_h's long K (= V) is cut into a fixed number of ranges
+ * chosen from (T, H, V) alone, whose fp32 sums are added in range order.
  *   lse_f32        device [T]: the forward's lse output
  *   grad_logp_f32  device [T]: upstream gradient of each logp
- *   grad_hidden_f32, grad_weight_f32: device, may be NULL (that product is skipped)
+ *   grad_hidden_f32, grad_weight_f32: device, 16-byte aligned, may be NULL (that
+ *                  product is skipped)
  *   workspace      device, 16-byte aligned, >= rlk_logprob_backward_workspace_size
- *                  bytes; holds dz as bf16 [T][V] row-major at offset 0 on return
- * Other arguments and conditions as rlk_logprob.  Asynchronous on `stream`.
- * The first call on a device creates a cuBLAS handle (kept until rlk_shutdown).
- * Deterministic run to run; unlike the forward, the gradients are not promised
- * to be independent of T (they are sums over rows and over the vocabulary).
+ *                  bytes; holds dz as bf16 [T][ldz] row-major at offset 0 on
+ *                  return, ldz = rlk_logprob_backward_dz_ld(V) = V rounded up to
+ *                  a multiple of 8 (the padding columns are unspecified)
+ * Other arguments and conditions as rlk_logprob.  Asynchronous on `stream`;
+ * allocates nothing.  Deterministic run to run and across GPUs of the same
+ * kind; unlike the forward, the gradients are not promised to be independent
+ * of T (they are sums over rows and over the vocabulary).
  */
 size_t rlk_logprob_backward_workspace_size(int64_t T, int64_t H, int64_t V);
+size_t rlk_logprob_backward_dz_ld(int64_t V);
 rlk_status rlk_logprob_backward(const void *hidden_bf16, const void *weight_bf16,
                                 const int32_t *targets_i32, const float *lse_f32,
                                 const float *grad_logp_f32, int64_t T, int64_t H, int64_t V,
@@ -404,6 +411,29 @@ rlk_status rlk_take_device_errors(rlk_stream_t stream, uint32_t *wait_error_bits
 rlk_status rlk_selftest_wait_timeout(const void *hidden_bf16, const void *weight_bf16,
                                      const int32_t *targets_i32, rlk_partial *partials,
                                      rlk_stream_t stream);
+
+/*
+ * The same self-test in the CTA-pair shape (the shape of every call with more
+ * than 128 rows): the forward kernel on a 256 x 512 x 256 problem, one pair of
+ * CTAs whose copies complete on the even CTA's barriers.
+ *   mode 1: the copy engine issues nothing; the even CTA's wait for data runs
+ *           out, every role sees the abort, and the pair's teardown hand-shake
+ *           finds nothing in flight.
+ *   mode 2: the MMA issuer consumes nothing; both CTAs fill their three-stage
+ *           rings with copies (which land), then their waits for a free stage
+ *           run out; the teardown hand-shake (the odd CTA reports its issued
+ *           stages to the even CTA, which waits until every copy of both CTAs
+ *           has landed before releasing it) drains them all.
+ * Either way the kernel records the timeout, releases its tensor memory and
+ * returns after about 2 s; rlk_check_device_error(stream) then returns
+ * RLK_ERR_TIMEOUT and the context stays usable.
+ *   hidden_bf16 [256][512], weight_bf16 [256][512] (16-byte aligned),
+ *   targets_i32 [256], partials (16-byte aligned, >= 256 * 16 bytes; left
+ *   unwritten): device buffers.  mode other than 1 or 2: RLK_ERR_INVALID_ARG.
+ */
+rlk_status rlk_selftest_wait_timeout_pair(const void *hidden_bf16, const void *weight_bf16,
+                                          const int32_t *targets_i32, rlk_partial *partials,
+                                          int mode, rlk_stream_t stream);
 
 /* Release the library's cached workspaces on every device it used (waits for
  * them to be idle).  Safe to call more than once. */

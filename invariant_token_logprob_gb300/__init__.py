@@ -18,7 +18,7 @@ from typing import Optional
 
 __all__ = ["RlkError", "lib", "logprob", "logprob_ws", "logprob_partials", "lse_merge",
            "consistency_stats", "workspace_size", "check_device_error", "take_device_errors", "vocab_tile", "row_tile",
-           "logprob_backward", "backward_workspace_size", "selected_token_logprob",
+           "logprob_backward", "backward_workspace_size", "backward_dz", "selected_token_logprob",
            "logprob_entropy", "entropy_workspace_size", "logprob_partials_shard",
            "lse_merge_sharded", "quantize_fp8_rows", "logprob_fp8", "fp8_workspace_size",
            "quantize_fp8_weight", "unpack_fp8_weight", "consistency_stats_async",
@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.rlk_consistency_stats_async.argtypes = [P, P, P, i64, P, P, sz, P]
         L.rlk_selftest_wait_timeout.restype = st
         L.rlk_selftest_wait_timeout.argtypes = [P, P, P, P, P]
+        L.rlk_selftest_wait_timeout_pair.restype = st
+        L.rlk_selftest_wait_timeout_pair.argtypes = [P, P, P, P, ctypes.c_int, P]
         L.rlk_check_device_error.restype = st
         L.rlk_check_device_error.argtypes = [P]
         L.rlk_take_device_errors.restype = st
@@ -110,6 +112,8 @@ def lib() -> ctypes.CDLL:
         L.rlk_logprob_entropy.argtypes = [P, P, P, i64, i64, i64, f32, P, P, P, P, P, sz, P]
         L.rlk_logprob_backward_workspace_size.restype = sz
         L.rlk_logprob_backward_workspace_size.argtypes = [i64, i64, i64]
+        L.rlk_logprob_backward_dz_ld.restype = sz
+        L.rlk_logprob_backward_dz_ld.argtypes = [i64]
         L.rlk_logprob_backward.restype = st
         L.rlk_logprob_backward.argtypes = [P, P, P, P, P, i64, i64, i64, f32, P, P, ctypes.c_int,
                                            P, sz, P]
@@ -327,11 +331,19 @@ def backward_workspace_size(T: int, H: int, V: int) -> int:
     return lib().rlk_logprob_backward_workspace_size(int(T), int(H), int(V))
 
 
+def backward_dz(workspace, T: int, V: int):
+    """The bf16 [T, V] view of dz inside a backward workspace (row stride
+    rlk_logprob_backward_dz_ld(V) elements)."""
+    import torch
+    ld = lib().rlk_logprob_backward_dz_ld(int(V))
+    return workspace[:T * ld * 2].view(torch.bfloat16).view(T, ld)[:, :V]
+
+
 def logprob_backward(h, W, targets, lse, grad_logp, inv_temp: float = 1.0, need_h: bool = True,
                      need_W: bool = True, grad_W=None, workspace=None, stream=None):
     """rlk_logprob_backward: returns (grad_h f32 [T,H] or None, grad_W f32 [V,H] or None,
-    workspace).  Pass grad_W to accumulate into it.  The workspace's first T*V*2 bytes
-    hold dz (bf16 [T,V]) afterwards."""
+    workspace).  Pass grad_W to accumulate into it.  dz (bf16 [T,V]) is left in the
+    workspace afterwards: backward_dz(workspace, T, V)."""
     import torch
     T, H, V = _check_inputs(h, W, targets)
     _need(lse, torch.float32, "lse", 1)

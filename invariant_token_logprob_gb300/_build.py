@@ -67,8 +67,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = LIB_PATH + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-lcublas",
-           "-Xlinker", "-rpath", "-Xlinker", "/usr/local/cuda/lib64", "-lpthread", "-ldl", "-lrt"]
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs,
+           "-lpthread", "-ldl", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stderr}")

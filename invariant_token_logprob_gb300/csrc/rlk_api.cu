@@ -105,18 +105,10 @@ EncodeTiledFn encode_fn() {
 // the matrix: bf16 (64 elements per box row) or 8-bit codes (128 elements).
 bool encode_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
                bool bytes) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
     const int esize = bytes ? 1 : 2;
-    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
-    const cuuint64_t strides[1] = {cuuint64_t(cols) * esize};
-    const cuuint32_t box[2] = {cuuint32_t(128 / esize), cuuint32_t(box_rows)};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                     2, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return rlk::encode_tensor_map_2d(map, base, uint64_t(cols), uint64_t(rows),
+                                     uint64_t(cols) * esize, uint32_t(128 / esize),
+                                     uint32_t(box_rows), bytes);
 }
 
 bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
@@ -173,6 +165,24 @@ rlk_status launch_partials(const void* h, const void* W, const int32_t* tg, int6
 }
 
 }  // namespace
+
+namespace rlk {
+bool encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                          uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                          bool bytes) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+    const cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
+    const cuuint32_t box[2] = {cuuint32_t(box_inner), cuuint32_t(box_outer)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+}  // namespace rlk
 
 extern "C" {
 
@@ -469,9 +479,20 @@ rlk_status rlk_logprob_entropy(const void* hidden_bf16, const void* weight_bf16,
                                                    out_entropy_f32, s));
 }
 
+namespace {
+size_t backward_dz_bytes(int64_t T, int64_t V) {
+    return (size_t(T) * size_t(rlk::backward_dz_ld(V)) * 2 + 255) / 256 * 256;
+}
+}  // namespace
+
 size_t rlk_logprob_backward_workspace_size(int64_t T, int64_t H, int64_t V) {
     if (T <= 0 || V <= 0 || H <= 0) return 0;
-    return (size_t(T) * size_t(V) * 2 + 15) / 16 * 16;
+    return backward_dz_bytes(T, V) + rlk::backward_split_bytes(T, H, V);
+}
+
+size_t rlk_logprob_backward_dz_ld(int64_t V) {
+    if (V <= 0) return 0;
+    return size_t(rlk::backward_dz_ld(V));
 }
 
 rlk_status rlk_logprob_backward(const void* hidden_bf16, const void* weight_bf16,
@@ -485,8 +506,8 @@ rlk_status rlk_logprob_backward(const void* hidden_bf16, const void* weight_bf16
     if (T == 0) return RLK_OK;
     if ((st = check_operands(hidden_bf16, weight_bf16, targets_i32, H)) != RLK_OK) return st;
     if (!lse_f32 || !grad_logp_f32) return RLK_ERR_INVALID_ARG;
-    if (!aligned4(lse_f32) || !aligned4(grad_logp_f32) || !aligned4(grad_hidden_f32) ||
-        !aligned4(grad_weight_f32))
+    if (!aligned4(lse_f32) || !aligned4(grad_logp_f32) || !aligned16(grad_hidden_f32) ||
+        !aligned16(grad_weight_f32))
         return RLK_ERR_ALIGNMENT;
     if (!workspace) return RLK_ERR_WORKSPACE;
     if (!aligned16(workspace)) return RLK_ERR_ALIGNMENT;
@@ -498,10 +519,13 @@ rlk_status rlk_logprob_backward(const void* hidden_bf16, const void* weight_bf16
     if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, &th, &tw)) != RLK_OK)
         return st;
     cudaError_t e = rlk::launch_lmhead_grad_logits(&th, &tw, targets_i32, lse_f32, grad_logp_f32,
-                                                   workspace, T, V, H, inv_temp, sms, s);
+                                                   workspace, rlk::backward_dz_ld(V), T, V, H,
+                                                   inv_temp, sms, s);
     if (e != cudaSuccess) return from_cuda(e);
+    void* split_ws = static_cast<char*>(workspace) + backward_dz_bytes(T, V);
     e = rlk::run_backward_gemms(hidden_bf16, weight_bf16, workspace, T, H, V, inv_temp,
-                                grad_hidden_f32, grad_weight_f32, accumulate_grad_weight != 0, s);
+                                grad_hidden_f32, grad_weight_f32, accumulate_grad_weight != 0,
+                                split_ws, sms, s);
     return from_cuda(e);
 }
 
@@ -562,7 +586,26 @@ rlk_status rlk_selftest_wait_timeout(const void* hidden_bf16, const void* weight
     if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, &th, &tw)) != RLK_OK)
         return st;
     return from_cuda(rlk::launch_lmhead_stall_selftest(&th, &tw, targets_i32, partials, T, V, H,
-                                                       sms, s));
+                                                       1, sms, s));
+}
+
+rlk_status rlk_selftest_wait_timeout_pair(const void* hidden_bf16, const void* weight_bf16,
+                                          const int32_t* targets_i32, rlk_partial* partials,
+                                          int mode, rlk_stream_t stream) {
+    constexpr int64_t T = 256, H = 512, V = 256;
+    if (mode != 1 && mode != 2) return RLK_ERR_INVALID_ARG;
+    rlk_status st = check_operands(hidden_bf16, weight_bf16, targets_i32, H);
+    if (st != RLK_OK) return st;
+    if (!partials) return RLK_ERR_INVALID_ARG;
+    if (!aligned16(partials)) return RLK_ERR_ALIGNMENT;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUtensorMap th, tw;
+    if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, &th, &tw)) != RLK_OK)
+        return st;
+    return from_cuda(rlk::launch_lmhead_stall_selftest(&th, &tw, targets_i32, partials, T, V, H,
+                                                       mode, sms, s));
 }
 
 rlk_status rlk_take_device_errors(rlk_stream_t stream, uint32_t* wait_error_bits,
@@ -572,9 +615,11 @@ rlk_status rlk_take_device_errors(rlk_stream_t stream, uint32_t* wait_error_bits
     if (st != RLK_OK) return st;
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return RLK_ERR_CUDA;
-    unsigned int word = 0;
+    unsigned int word = 0, word_bwd = 0;
     unsigned long long rows = 0;
     if (rlk::lmhead_take_error(&word) != cudaSuccess) return RLK_ERR_CUDA;
+    if (rlk::bwd_gemm_take_error(&word_bwd) != cudaSuccess) return RLK_ERR_CUDA;
+    word |= word_bwd;
     if (rlk::take_target_range_rows(&rows) != cudaSuccess) return RLK_ERR_CUDA;
     if (wait_error_bits) *wait_error_bits = word;
     if (target_range_rows) *target_range_rows = rows;
@@ -604,7 +649,6 @@ rlk_status rlk_shutdown(void) {
     }
     g_ws.clear();
     if (have_prev) cudaSetDevice(prev);
-    rlk::release_backward_handles();
     return st;
 }
 

@@ -27,6 +27,13 @@ int lmhead_w_box_rows(int64_t T);
 // memory held and are never reported.
 int lmhead_a_box_rows(int64_t T);
 
+// 2-D TMA tensor map, 128-byte swizzle, zero fill outside the matrix: `outer`
+// rows of `inner` elements (bf16, or bytes when `bytes`), row_bytes apart
+// (a multiple of 16), boxes of box_inner x box_outer elements (box_inner *
+// element size <= 128).  False if the driver refuses it.
+bool encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                          uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool bytes);
+
 // The smallest h box the LM-head kernel copies (rows); see lmhead_a_box_rows.
 constexpr int kMinTmaRows = 16;
 
@@ -52,18 +59,30 @@ cudaError_t launch_lse_merge_sharded(const void* partials, int nvt_shard,
 
 // Same main loop with the backward epilogue: recomputes the logits and writes
 // dz[t][v] = grad[t] * ([v == target[t]] - exp(z[t][v] - lse[t])) as bf16
-// (0 for rows whose target lies outside [0, V)); dz is [T][V] row-major.
+// (0 for rows whose target lies outside [0, V)); dz is [T][ldz] row-major with
+// ldz = backward_dz_ld(V) (rows start on 16-byte boundaries, as TMA needs).
 cudaError_t launch_lmhead_grad_logits(const CUtensorMap* th, const CUtensorMap* tw,
                                       const int32_t* targets, const float* lse, const float* grad,
-                                      void* dz, int64_t T, int64_t V, int64_t H, float inv_temp,
-                                      int num_sms, cudaStream_t stream);
+                                      void* dz, int64_t ldz, int64_t T, int64_t V, int64_t H,
+                                      float inv_temp, int num_sms, cudaStream_t stream);
+
+// Row stride (elements) of dz: V rounded up to a multiple of 8.
+int64_t backward_dz_ld(int64_t V);
+// Workspace bytes the grad_h product needs for its K-range partial sums (0 if
+// it runs as one range); a function of the shape alone.
+size_t backward_split_bytes(int64_t T, int64_t H, int64_t V);
 
 // grad_h [T][H] = inv_temp * dz . W and grad_W [V][H] (+)= inv_temp * dz^T . h
-// with fp32 accumulation (library GEMMs; either output may be null).
-cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, int64_t T,
-                               int64_t H, int64_t V, float inv_temp, float* grad_h,
-                               float* grad_W, bool accumulate_W, cudaStream_t stream);
-void release_backward_handles();
+// with fp32 accumulation on the tensor cores (either output may be null);
+// dz [T][backward_dz_ld(V)] bf16; split_ws holds backward_split_bytes(T, H, V)
+// bytes (16-byte aligned, as are grad_h and grad_W).
+cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, int64_t T, int64_t H,
+                               int64_t V, float inv_temp, float* grad_h, float* grad_W,
+                               bool accumulate_W, void* split_ws, int num_sms,
+                               cudaStream_t stream);
+// Reads and clears the backward GEMM kernel's per-device error word (bit 0: a
+// bounded wait ran out; bit 1: a teardown wait ran out).
+cudaError_t bwd_gemm_take_error(unsigned int* out);
 
 // FP8 (e4m3) operands: th maps row-major uint8 codes [h_rows][H] with boxes
 // {2*kKBlock, kRowTile}; tw maps the tile-packed weight as
@@ -87,12 +106,15 @@ cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_ro
 cudaError_t launch_quantize_fp8_weight_tiled(const void* W, int64_t V, int64_t H, void* packed,
                                              float* scales, cudaStream_t stream);
 
-// Bounded-wait self-test: the forward kernel with its producer issuing no
-// copies, so the MMA warp's wait runs out (kernel error word bit 0) after its
-// time limit and every role returns.
+// Bounded-wait self-test of the forward kernel (single CTA for T <= 128, CTA
+// pair above): mode 1, its producer issues no copies, so the MMA warp's wait
+// runs out; mode 2, its MMA issuer consumes no stage, so the producers fill
+// the ring and their waits for a free stage run out.  Either way the kernel
+// error word gets bit 0 after the time limit and every role returns.
 cudaError_t launch_lmhead_stall_selftest(const CUtensorMap* th, const CUtensorMap* tw,
                                          const int32_t* targets, void* partials, int64_t T,
-                                         int64_t V, int64_t H, int num_sms, cudaStream_t stream);
+                                         int64_t V, int64_t H, int mode, int num_sms,
+                                         cudaStream_t stream);
 
 // Reads and clears the per-device error word of the LM-head kernel (bit 0: a
 // bounded wait ran out).  Synchronous on the current device.

@@ -79,9 +79,15 @@ struct Pipe {
     static constexpr int kKbPerStage = kPair ? 2 : 1;     // k-blocks per stage (one barrier)
     static constexpr int kStageBytes = kKbPerStage * kKbBytes;
     static constexpr int kStages = kPair ? 3 : 4;
-    static constexpr int kBarriers = 2 * kStages + 2 * kAccBufs + 1;
+    // full / empty per stage, tfull / tempty per accumulator, drain, and for the
+    // CTA pair's teardown hand-shake odd_done (even CTA) and drained (odd CTA)
+    static constexpr int kBarriers = 2 * kStages + 2 * kAccBufs + 3;
+    // after the barriers: TMEM slot, abort flag, the odd CTA's issue count and
+    // its bytes per stage slot (written into the even CTA's words at teardown)
+    static constexpr int kWords = 3 + kStages;
     static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ +
-                                         size_t(kStages) * kStageBytes + kBarriers * 8 + 16;
+                                         size_t(kStages) * kStageBytes + kBarriers * 8 +
+                                         kWords * 4 + 16;
     static constexpr int kMmaM = kPair ? 2 * kBM : kBM;
     static constexpr int kEpiArrivals = kPair ? 8 : 4;  // epilogue warps releasing a buffer
     static_assert(kStageBytes % 1024 == 0, "stage tiles 1024-B aligned");
@@ -89,6 +95,7 @@ struct Pipe {
 };
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for teardown waits
+constexpr uint64_t kPeerLimitNs = 8000000000ull;  // waits on the other CTA's teardown
 
 static_assert(kBK * 2 == 128, "one k-block is one 128-byte swizzle row");
 static_assert(kABytes % 1024 == 0, "stage tiles 1024-B aligned");
@@ -102,7 +109,8 @@ struct Args {
     float* ent_u;          // mode 2: [T][num_n] sum exp(z - m) (z - m) per tile
     const float* lse;      // mode 1: forward LSE per row
     const float* grad;     // mode 1: upstream gradient of logp per row
-    uint16_t* dz;          // mode 1: [T][V] bf16 gradient of logp w.r.t. the logits
+    uint16_t* dz;          // mode 1: [T][ldz] bf16 gradient of logp w.r.t. the logits
+    int64_t ldz;           // mode 1: row stride of dz (a multiple of 8 elements)
     int64_t T;
     int64_t h_rows; // rows the h tensor map covers (>= T; padded copies are longer)
     int a_rows;     // rows of each h box (lmhead_a_box_rows(T))
@@ -115,7 +123,8 @@ struct Args {
     int band;    // row units per raster band (schedule only; never affects values)
     int num_tiles;
     float inv_temp;
-    int stall_selftest;  // 1: the producer issues no copies (bounded-wait self-test)
+    int stall_selftest;  // bounded-wait self-test: 1, the producer issues no copies;
+                         // 2, the MMA issuer consumes no stage
     const float* sh;     // fp8 operands: per-row scale of h [rows]
     const float* sw;     // fp8 operands: per-row scale of W [V] (this launch's rows)
 };
@@ -165,15 +174,18 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
-// Teardown wait: bounded, ignores the abort flag.
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+// Teardown wait: bounded, ignores the abort flag; false if the limit ran out.
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity,
+                                           uint64_t limit_ns = kDrainLimitNs) {
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kDrainLimitNs) {
+    while (!try_wait_scoped<kCluster>(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(&g_lmhead_error, 2u);
-            return;
+            return false;
         }
     }
+    return true;
 }
 
 // Epilogue modes of the one kernel: the main loop is shared, so the logits a
@@ -223,12 +235,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBarriers);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // tmem_slot[2]: the odd CTA's issue count; tmem_slot[3 + s]: its bytes in slot s
+    volatile uint32_t* odd_words = tmem_slot + 2;
 
     auto full_bar = [&](int s) { return smem_u32(bars + s); };
     auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
     auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * kStages + b); };
     auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * kStages + kAccBufs + b); };
     const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 2 * kAccBufs);
+    const uint32_t odd_done_bar = drain_bar + 8;  // even CTA: the odd CTA stopped issuing
+    const uint32_t drained_bar = drain_bar + 16;  // odd CTA: every copy of the pair landed
     // k-block j of stage s: h block, then W block
     auto a_tile = [&](int s, int j) {
         return tiles_addr + uint32_t(s) * kStageBytes + uint32_t(j) * P::kKbBytes;
@@ -249,6 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tempty_bar(b), P::kEpiArrivals);  // one arrival per epilogue warp
         }
         mbar_init(drain_bar, 1);
+        mbar_init(odd_done_bar, 1);
+        mbar_init(drained_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -282,9 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
-            // Self-test: no copy is ever issued, so the MMA warp's first wait can
+            uint32_t slot_bytes_odd[kStages];  // CTA pair: odd CTA's bytes of the last issue per slot
+#pragma unroll
+            for (int i = 0; i < kStages; ++i) slot_bytes_odd[i] = 0;
+            // Self-test 1: no copy is ever issued, so the MMA warp's first wait can
             // only end by running out; everything else then sees the abort flag.
-            const int ntiles = p.stall_selftest ? 0 : p.num_tiles;
+            const int ntiles = p.stall_selftest == 1 ? 0 : p.num_tiles;
             for (int tile = slot; ok && tile < ntiles; tile += nslots) {
                 int mu, n;
                 tile_coords(p, tile, mu, n);
@@ -292,16 +313,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tile of the last unit) or of W (odd half of the last vocabulary
                 // tile) is not copied; the MMA then reads stale shared memory for
                 // rows / columns that the epilogues never report.
-                // per k-block: single CTA, its h box and W block; CTA pair, both CTAs
-                uint32_t kb_bytes = uint32_t(p.a_rows) * 128u + P::kBBytes;
+                // per k-block: single CTA, its h box and W block; CTA pair, each CTA's
+                uint32_t bytes_r[2] = {uint32_t(p.a_rows) * 128u + P::kBBytes, 0u};
                 bool load_a = true, load_b = true;
                 if constexpr (kPair) {
-                    kb_bytes = 0;
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         const bool la = int64_t(2 * mu + r) * kBM < p.h_rows;
                         const bool lb = n * kBN + r * P::kBRows < p.V;
-                        kb_bytes += (la ? kABytes : 0) + (lb ? P::kBBytes : 0);
+                        bytes_r[r] = (la ? kABytes : 0) + (lb ? P::kBBytes : 0);
                         if (uint32_t(r) == rank) {
                             load_a = la;
                             load_b = lb;
@@ -319,7 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (kPair) {
                         // both CTAs' copies complete on the even CTA's stage barrier
                         const uint32_t fb = mapa_shared(full_bar(stage), 0);
-                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), nkb * kb_bytes);
+                        slot_bytes_odd[stage] = uint32_t(nkb) * bytes_r[1];
+                        if (rank == 0)
+                            mbar_arrive_expect_tx(full_bar(stage),
+                                                  uint32_t(nkb) * (bytes_r[0] + bytes_r[1]));
                         for (int j = 0; j < nkb; ++j) {
                             const int kb = kb0 + j;
                             if (load_a)
@@ -336,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     } else {
-                        mbar_arrive_expect_tx(full_bar(stage), nkb * kb_bytes);
+                        mbar_arrive_expect_tx(full_bar(stage), uint32_t(nkb) * bytes_r[0]);
                         for (int j = 0; j < nkb; ++j) {
                             const int kb = kb0 + j;
                             tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage, j), kb * kBKE,
@@ -356,19 +379,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!ok) {
+            if constexpr (!kPair) {
                 // Let the copies this thread started land before the CTA exits.
-                if (!kPair || rank == 0) {
+                if (!ok) {
                     const int first = issued > kStages ? issued - kStages : 0;
                     for (int i = first; i < issued; ++i)
                         wait_drain(full_bar(i % kStages), uint32_t(i / kStages) & 1u);
-                } else {
-                    // the odd CTA's copies signal the even CTA's barriers, which
-                    // it cannot wait on: give them a fixed time to land
+                }
+            } else if (rank == 1) {
+                // Teardown hand-shake (normal path too, where it finds every copy
+                // landed).  The odd CTA's copies complete on the even CTA's
+                // barriers, which it cannot wait on: it hands the even CTA its
+                // issue count and per-slot bytes, then waits for the all-clear.
+                st_shared_cluster_u32(mapa_shared(smem_u32(tmem_slot + 2), 0), uint32_t(issued));
+#pragma unroll
+                for (int i = 0; i < kStages; ++i)
+                    st_shared_cluster_u32(mapa_shared(smem_u32(tmem_slot + 3 + i), 0),
+                                          slot_bytes_odd[i]);
+                mbar_arrive_cluster(mapa_shared(odd_done_bar, 0));  // release: stores first
+                if (!wait_drain<true>(drained_bar, 0, kPeerLimitNs)) {
+                    // the even CTA never answered: give the copies a fixed time
                     const uint64_t t0 = global_timer_ns();
                     while (global_timer_ns() - t0 < 1000000ull) {
                     }
                 }
+            } else {
+                // Even CTA: every stage either CTA issued must complete before the
+                // pair leaves.  The last kStages issues may be incomplete; a
+                // stage issued by one CTA only is completed by hand (the odd CTA's
+                // copies never expected here: arrive.expect_tx; copies expected
+                // from the odd CTA that it never issued: complete_tx).
+                if (wait_drain<true>(odd_done_bar, 0, kPeerLimitNs)) {
+                    const int odd_issued = int(odd_words[0]);
+                    const int maxi = max(issued, odd_issued);
+                    for (int i = max(0, maxi - kStages); i < maxi; ++i) {
+                        const int sl = i % kStages;
+                        if (i >= issued)
+                            mbar_arrive_expect_tx(full_bar(sl), odd_words[1 + sl]);
+                        else if (i >= odd_issued)
+                            mbar_complete_tx(full_bar(sl), slot_bytes_odd[sl]);
+                        wait_drain(full_bar(sl), uint32_t(i / kStages) & 1u);
+                    }
+                }
+                mbar_arrive_cluster(mapa_shared(drained_bar, 1));
             }
         }
         __syncwarp();
@@ -378,7 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int tile = slot; ok && tile < p.num_tiles; tile += nslots) {
+            // Self-test 2: no stage is consumed, so the producers fill the ring,
+            // then wait for a free stage until their limit runs out.
+            const int ntiles = p.stall_selftest == 2 ? 0 : p.num_tiles;
+            for (int tile = slot; ok && tile < ntiles; tile += nslots) {
                 if (!wait_bounded<kPair>(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * uint32_t(kBN);
@@ -549,8 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = live && tgt >= 0 && tgt < p.V;
                 const float g = valid ? __ldg(p.grad + row) : 0.0f;
                 const float lse2 = live ? __ldg(p.lse + row) * kLog2e : 0.0f;
-                uint16_t* dz_row = p.dz + (live ? row : 0) * int64_t(p.V);
-                const bool vec_ok = (p.V & 7) == 0;  // rows start on 16-byte boundaries
+                uint16_t* dz_row = p.dz + (live ? row : 0) * p.ldz;  // 16-byte aligned rows
                 for (int c = 0; c < nchunks; ++c) {
                     uint32_t r[32];
                     tmem_ld32(t_addr + uint32_t(c * 32), r);
@@ -570,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         packed[j / 2] = pack_bf16x2(d0, d1);
                     }
                     const int nvalid = ncols - c * 32;
-                    if (live && nvalid >= 32 && vec_ok) {
+                    if (live && nvalid >= 32) {
                         uint4* dst = reinterpret_cast<uint4*>(dz_row + cbase);
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4)
@@ -687,7 +742,7 @@ cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, in
                         int num_sms, cudaStream_t stream) {
     if (a.h_rows == 0) a.h_rows = a.T;
     a.a_rows = lmhead_a_box_rows(a.T);
-    if (lmhead_use_pair(a.T) && !a.stall_selftest)
+    if (lmhead_use_pair(a.T))
         return launch_variant<kMode, kFp8, true>(th, tw, a, H, num_sms, stream);
     return launch_variant<kMode, kFp8, false>(th, tw, a, H, num_sms, stream);
 }
@@ -741,26 +796,28 @@ cudaError_t launch_lmhead_partials_fp8(const CUtensorMap* th, const CUtensorMap*
 
 cudaError_t launch_lmhead_stall_selftest(const CUtensorMap* th, const CUtensorMap* tw,
                                          const int32_t* targets, void* partials, int64_t T,
-                                         int64_t V, int64_t H, int num_sms, cudaStream_t stream) {
+                                         int64_t V, int64_t H, int mode, int num_sms,
+                                         cudaStream_t stream) {
     Args a = {};
     a.targets = targets;
     a.partials = static_cast<float4*>(partials);
     a.T = T;
     a.V = int(V);
     a.inv_temp = 1.0f;
-    a.stall_selftest = 1;
+    a.stall_selftest = mode;
     return launch_mode<kModePartials>(th, tw, a, H, num_sms, stream);
 }
 
 cudaError_t launch_lmhead_grad_logits(const CUtensorMap* th, const CUtensorMap* tw,
                                       const int32_t* targets, const float* lse, const float* grad,
-                                      void* dz, int64_t T, int64_t V, int64_t H, float inv_temp,
-                                      int num_sms, cudaStream_t stream) {
+                                      void* dz, int64_t ldz, int64_t T, int64_t V, int64_t H,
+                                      float inv_temp, int num_sms, cudaStream_t stream) {
     Args a = {};
     a.targets = targets;
     a.lse = lse;
     a.grad = grad;
     a.dz = static_cast<uint16_t*>(dz);
+    a.ldz = ldz;
     a.T = T;
     a.V = int(V);
     a.inv_temp = inv_temp;

@@ -114,6 +114,19 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
+// Perform the completion of `bytes` transaction bytes on a local mbarrier
+// without a copy: accounts for copies that were expected on the barrier but
+// will never be issued (used only when tearing a pipeline down).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// 32-bit store to the shared memory of any CTA of the cluster (address from mapa).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(desc) : "memory");
@@ -225,6 +238,23 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major bf16 operand tile written by
+// TMA with 128-byte swizzling: each 128-byte row holds 64 consecutive M (or N)
+// elements of one k; 8 consecutive k rows form a 1024-byte swizzle atom.  In
+// the descriptor (same fields as above) the leading byte offset is the distance
+// between atoms along M/N (the next 64 elements of M/N), the stride byte offset
+// the distance between atoms along K (the next 8 k).  Atoms are 1024-B aligned.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t lbo_bytes,
+                                                       uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
 // Instruction descriptor for tcgen05.mma kind::f16 with bf16 A/B, fp32 D, both
 // operands K-major, dense: [4,6) D format 1 = f32; [7,10) A format 1 = bf16;
 // [10,13) B format 1 = bf16; bit 15/16 = 0 (K-major); [17,23) N >> 3;
@@ -232,6 +262,12 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same with the operands' majorness given: bit 15 set = A MN-major, bit 16
+// set = B MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_major(int M, int N, bool a_mn, bool b_mn) {
+    return idesc_bf16_f32(M, N) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by a single thread.  kGroup 2: the

@@ -3,7 +3,7 @@
 Error model, from the arithmetic of the CUDA path: the logits are the
 forward's fp32 logits, p = exp(z - lse) in fp32 (relative error ~1e-6), dz is
 rounded once to bf16 (relative error <= 2^-9), and the two products are bf16 x
-bf16 -> fp32 GEMMs.  So, elementwise,
+bf16 -> fp32 tensor-core GEMMs of the library.  So, elementwise,
   |dz_gpu - dz|  <= 2^-8 |dz| + 2e-5 |g|
   |dh_gpu - dh|  <= inv_temp 2^-7 sum_v |dz[t,v]| |W[v,k]| + 1e-6
   |dW_gpu - dW|  <= inv_temp 2^-7 sum_t |dz[t,v]| |h[t,k]| + 1e-6
@@ -39,8 +39,7 @@ def _run(d, grad, it, need_h=True, need_W=True, grad_W=None):
                                       need_h=need_h, need_W=need_W, grad_W=grad_W)
     rlk.check_device_error()
     T, V = d["h"].shape[0], d["W"].shape[0]
-    dz = ws[:T * V * 2].view(torch.bfloat16).view(T, V)
-    return gh, gW, dz
+    return gh, gW, rlk.backward_dz(ws, T, V)
 
 
 def _check(d, grad, it, gh, gW, dz, what):
@@ -72,6 +71,34 @@ def test_backward_matches_oracle(T, H, V, seed):
     gh, gW, dz = _run(d, grad, it)
     _check(d, grad, it, gh, gW, dz, f"T={T} H={H} V={V}")
     assert torch.all(dz[0] == 0) and torch.all(gh[0] == 0)
+
+
+@pytest.mark.parametrize("T,H,V,it", [
+    (40, 192, 20000, 1.0),                     # grad_h in 8 K ranges; H one ragged unit
+    (300, 320, 3001, float(np.float32(1 / 0.7))),  # ragged T (2 pair units), H, V, k-blocks
+    (257, 256, 70000, 1.0),                    # odd row tile of the last pair unit alone
+    (7, 64, 129, 2.0),                         # smaller than one tile everywhere
+])
+def test_gemms_match_fp64_products_of_the_kernels_dz(T, H, V, it):
+    """The two tensor-core products alone, against fp64 products of the dz the
+    dz kernel wrote (so the bf16 rounding of dz is not part of the error): each
+    element is an fp32 sum of exact bf16 products, so |error| stays within
+    2^-13 of sum |terms| (the sum order is fixed but not the fp64 one); a wrong
+    operand, index or k step would be off by O(1) of it."""
+    import invariant_token_logprob_gb300 as rlk
+    d = to_dev(lm_head_inputs(T, H, V, seed=T + V, hidden="normal", w_std=0.05))
+    grad = torch.randn(T, device="cuda", generator=torch.Generator("cuda").manual_seed(T))
+    base = torch.randn(V, H, device="cuda", generator=torch.Generator("cuda").manual_seed(V))
+    gh, gW, dz = _run(d, grad, it, grad_W=base.clone())
+    dz64 = dz.double().cpu()
+    W64, h64 = d["W"].double().cpu(), d["h"].double().cpu()
+    t = float(np.float32(it))
+    ref_h = t * (dz64 @ W64)
+    bound_h = 2.0 ** -13 * t * (dz64.abs() @ W64.abs()) + 1e-30
+    assert torch.all((gh.double().cpu() - ref_h).abs() <= bound_h), "grad_h"
+    ref_W = base.double().cpu() + t * (dz64.T @ h64)
+    bound_W = 2.0 ** -13 * (base.double().cpu().abs() + t * (dz64.abs().T @ h64.abs())) + 1e-30
+    assert torch.all((gW.double().cpu() - ref_W).abs() <= bound_W), "grad_W (accumulated)"
 
 
 def test_backward_accumulates_and_skips():
@@ -133,7 +160,7 @@ def test_backward_full_size_sampled_rows_and_invariant():
     Wf = d["W"].float().cpu().numpy().astype(np.float64)
     bh = 2.0 ** -7 * (np.abs(sub["dz"]) @ np.abs(Wf)) + 1e-6
     assert np.all(np.abs(gh[rows].cpu().numpy() - sub["dh"]) <= bh)
-    dz = ws[:T * V * 2].view(torch.bfloat16).view(T, V)
+    dz = rlk.backward_dz(ws, T, V)
     dzf = dz[rows].float().cpu().numpy().astype(np.float64)
     assert np.all(np.abs(dzf - sub["dz"]) <= 2.0 ** -8 * np.abs(sub["dz"]) +
                   2e-5 * np.abs(grad[rows].cpu().numpy())[:, None])

@@ -2,8 +2,11 @@
 
 * A device-side wait that nothing will ever complete runs out after its time
   limit; the kernel records it, frees its tensor memory and returns, the host
-  reads RLK_ERR_TIMEOUT, and the CUDA context stays usable (no fault, no hang:
-  the self-test issues no copy at all).
+  reads RLK_ERR_TIMEOUT, and the CUDA context stays usable (no fault, no hang).
+  Single-CTA shape: the self-test issues no copy at all.  CTA-pair shape: the
+  same (mode 1), and a run whose MMA issuer consumes nothing (mode 2), so both
+  CTAs' copies fill their rings and the pair's teardown hand-shake must drain
+  them before the CTAs leave.
 * rlk_logprob_ws captured in a CUDA graph and replayed with new inputs gives
   the eager bits (decode loops run under CUDA graphs).
 * Concurrent calls on two streams (each with its own cached workspace) give
@@ -61,6 +64,43 @@ def test_bounded_wait_runs_out_and_context_survives(olib):
     dd = to_dev(d)
     gpu = gpu_logprob(dd["h"], dd["W"], dd["targets"])
     assert_parity(gpu, oracle.logprob(d["h"], d["W"], d["targets"], lib=olib), what="after timeout")
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_pair_shape_bounded_wait_runs_out_and_context_survives(olib, mode):
+    import invariant_token_logprob_gb300 as rlk
+    L = rlk.lib()
+    g = torch.Generator("cuda").manual_seed(mode)
+    h = torch.randn(256, 512, device="cuda", generator=g).to(torch.bfloat16)
+    W = torch.randn(256, 512, device="cuda", generator=g).to(torch.bfloat16)
+    tg = torch.zeros(256, device="cuda", dtype=torch.int32)
+    part = torch.full((256 * 4,), 7.0, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rlk.check_device_error()
+    assert L.rlk_selftest_wait_timeout_pair(ctypes.c_void_p(h.data_ptr()),
+                                            ctypes.c_void_p(W.data_ptr()),
+                                            ctypes.c_void_p(tg.data_ptr()),
+                                            ctypes.c_void_p(part.data_ptr()), 3, stream) == 1
+    t0 = time.time()
+    st = L.rlk_selftest_wait_timeout_pair(ctypes.c_void_p(h.data_ptr()),
+                                          ctypes.c_void_p(W.data_ptr()),
+                                          ctypes.c_void_p(tg.data_ptr()),
+                                          ctypes.c_void_p(part.data_ptr()), mode, stream)
+    assert st == 0
+    bits, rows = rlk.take_device_errors()
+    elapsed = time.time() - t0
+    assert bits & 1, bits  # a wait ran out
+    assert not bits & 2, bits  # and every teardown wait (the hand-shake, the drains) ended in time
+    assert 1.0 < elapsed < 30.0, elapsed
+    assert torch.all(part == 7.0)  # nothing was written
+    rlk.check_device_error()
+    # the context is still usable: CTA-pair and single-CTA calls are correct
+    for T in (300, 20):
+        d = lm_head_inputs(T, 128, 900, seed=T)
+        dd = to_dev(d)
+        gpu = gpu_logprob(dd["h"], dd["W"], dd["targets"])
+        assert_parity(gpu, oracle.logprob(d["h"], d["W"], d["targets"], lib=olib),
+                      what=f"after pair timeout, T={T}")
 
 
 @pytest.mark.parametrize("T", [1, 37, 300])  # 300: CTA-pair clusters, ragged last unit
