@@ -94,6 +94,10 @@ def parse():
                    help="time only the decode regime at T = --decode-T (for profiling)")
     p.add_argument("--decode-T", type=int, default=1)
     p.add_argument("--fp8", action="store_true", help="decode-only: the FP8 (e4m3 W) variant")
+    p.add_argument("--backward-only", action="store_true",
+                   help="time only rlk_logprob_backward (T=4096, H=4096, V=--bwd-V) per product "
+                        "(for profiling)")
+    p.add_argument("--bwd-V", type=int, default=V_CFG)
     return p.parse_args()
 
 
@@ -748,12 +752,73 @@ def run_ours(args):
     return 0
 
 
+def run_backward_only(args):
+    """rlk_logprob_backward alone on T=4096, H=4096, V=--bwd-V: per call the dz
+    kernel alone, dz + grad_W, dz + grad_h and dz + both, interleaved over
+    rounds (CUDA events, median per case); prints one JSON line.  Used for
+    profiling the backward's kernels."""
+    import torch
+    import invariant_token_logprob_gb300 as rlk
+    from invariant_token_logprob_gb300.inputs import lm_head_inputs
+    torch.cuda.set_device(0)
+    pk = peaks()
+    T, H, V = T_CFG, H_CFG, args.bwd_V
+    d = lm_head_inputs(T, H, V, seed=1000, device="cuda", hidden="rms")
+    h, W, tg = d["h"], d["W"], d["targets"]
+    lp, lse, am = rlk.logprob(h, W, tg, 1.0)
+    grad = torch.ones(T, device="cuda")
+    ws = torch.empty(rlk.backward_workspace_size(T, H, V), dtype=torch.uint8, device="cuda")
+    gh = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    gW = torch.empty((V, H), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    L = rlk.lib()
+    import ctypes
+
+    def call(need_h, need_W):
+        st = L.rlk_logprob_backward(
+            ctypes.c_void_p(h.data_ptr()), ctypes.c_void_p(W.data_ptr()),
+            ctypes.c_void_p(tg.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+            ctypes.c_void_p(grad.data_ptr()), T, H, V, ctypes.c_float(1.0),
+            ctypes.c_void_p(gh.data_ptr()) if need_h else None,
+            ctypes.c_void_p(gW.data_ptr()) if need_W else None, 0,
+            ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.c_void_p(stream.cuda_stream))
+        assert st == 0, st
+
+    cases = {"dz": (False, False), "dz+grad_W": (False, True), "dz+grad_h": (True, False),
+             "all": (True, True)}
+    for c in cases.values():
+        for _ in range(args.warmup):
+            call(*c)
+    times = {k: [] for k in cases}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        for k, c in cases.items():
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(args.steps):
+                call(*c)
+            e1.record(stream)
+            e1.synchronize()
+            times[k].append(e0.elapsed_time(e1) / args.steps)
+    rlk.check_device_error()
+    med = {k: statistics.median(v) for k, v in times.items()}
+    fl = 2.0 * T * H * V
+    res = dict(mode="backward-only", T=T, H=H, V=V, ms=med,
+               grad_W_ms=med["dz+grad_W"] - med["dz"], grad_h_ms=med["dz+grad_h"] - med["dz"])
+    res["grad_W_frac"] = fl / (res["grad_W_ms"] * 1e-3) / 1e12 / pk["bf16_tflops"]
+    res["grad_h_frac"] = fl / (res["grad_h_ms"] * 1e-3) / 1e12 / pk["bf16_tflops"]
+    print(json.dumps(res), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.decode_only:
         return run_decode_only(args)
+    if args.backward_only:
+        return run_backward_only(args)
     return run_ours(args)
 
 

@@ -60,6 +60,11 @@ def _bind(lib):
     lib.oracle_logprob_fp8.restype = ctypes.c_int
     lib.oracle_logprob_fp8.argtypes = [P, P, P, P, P, i64, i64, i64, ctypes.c_float, P, i64,
                                        P, P, P, P]
+    lib.oracle_quantize_fp8_blocks.restype = ctypes.c_int
+    lib.oracle_quantize_fp8_blocks.argtypes = [P, i64, i64, i64, P, P]
+    lib.oracle_logprob_fp8_block.restype = ctypes.c_int
+    lib.oracle_logprob_fp8_block.argtypes = [P, P, P, P, P, i64, i64, i64, ctypes.c_float, P, i64,
+                                             P, P, P, P]
     lib.oracle_logprob_f64.restype = ctypes.c_int
     lib.oracle_logprob_f64.argtypes = [P, P, P, i64, i64, i64, ctypes.c_double, P, P]
     return lib
@@ -281,4 +286,45 @@ def logprob_fp8(qh, sh, qw, sw, targets, inv_temp: float = 1.0, rows=None, lib=N
                                 _ptr(out["lse"]), _ptr(out["argmax"]), _ptr(out["top2gap"]))
     if rc != 0:
         raise ValueError("oracle_logprob_fp8 rejected its arguments")
+    return out
+
+
+def quantize_fp8_blocks(x, block_rows: int, lib=None):
+    """Block e4m3 quantisation of bf16 bits [rows, H] in block_rows x 128 blocks:
+    returns (codes uint8 [rows, H], scales float32 [ceil(rows/block_rows), ceil(H/128)])."""
+    lib = lib or load()
+    x = _u16(x)
+    rows, H = x.shape
+    nkb = (H + 127) // 128
+    nrb = (rows + block_rows - 1) // block_rows
+    codes = np.zeros((rows, H), dtype=np.uint8)
+    scales = np.zeros((nrb, nkb), dtype=np.float32)
+    if lib.oracle_quantize_fp8_blocks(_ptr(x), rows, H, int(block_rows), _ptr(codes),
+                                      _ptr(scales)) != 0:
+        raise ValueError("oracle_quantize_fp8_blocks rejected its arguments")
+    return codes, scales
+
+
+def logprob_fp8_block(qh, sh, qw, sw, targets, inv_temp: float = 1.0, rows=None, lib=None) -> dict:
+    """Oracle logprob from block-quantised operands: qh [T,H] / sh [T, ceil(H/128)]
+    (1 x 128 blocks), qw [V,H] / sw [ceil(V/128), ceil(H/128)] (128 x 128 blocks)."""
+    lib = lib or load()
+    qh = np.ascontiguousarray(qh, dtype=np.uint8)
+    qw = np.ascontiguousarray(qw, dtype=np.uint8)
+    sh = np.ascontiguousarray(sh, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    tg = _i32(targets)
+    T, H = qh.shape
+    V = qw.shape[0]
+    nkb = (H + 127) // 128
+    assert qw.shape[1] == H and sh.shape == (T, nkb) and sw.shape == ((V + 127) // 128, nkb)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = T if r is None else r.shape[0]
+    out = {k: np.zeros(n, dtype=np.float64) for k in ("logp", "lse", "top2gap")}
+    out["argmax"] = np.zeros(n, dtype=np.int64)
+    if lib.oracle_logprob_fp8_block(_ptr(qh), _ptr(sh), _ptr(qw), _ptr(sw), _ptr(tg), T, H, V,
+                                    ctypes.c_float(inv_temp), _ptr(r), n, _ptr(out["logp"]),
+                                    _ptr(out["lse"]), _ptr(out["argmax"]),
+                                    _ptr(out["top2gap"])) != 0:
+        raise ValueError("oracle_logprob_fp8_block rejected its arguments")
     return out

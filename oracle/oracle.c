@@ -637,3 +637,111 @@ int oracle_logprob_fp8(const uint8_t *qh, const float *sh, const uint8_t *qw, co
     }
     return bad ? -1 : 0;
 }
+
+
+/* ------------------------------------------------------------------------
+ * Block-scaled FP8 (W8A8) variant.  The consistency blog's dense layers use
+ * block-FP8 weights in DeepGEMM's W8A8 batch-invariant mode ("Finish RL
+ * Training Faster ...", section on the dense GEMM: FP8 computation with one
+ * fixed reduction order; RNE quantisation).  The page gives no block shape
+ * for an LM head; the reading taken is DeepGEMM's: activations in 1 x 128
+ * blocks (one token, 128 consecutive k) and weights in 128 x 128 blocks (128
+ * vocabulary rows, 128 consecutive k).  Per block s = amax / 448 in fp32
+ * (1 for an all-zero block) and code = RNE-to-e4m3(x / s), fp32 division.
+ * The logit is the sum over k blocks b of each block's code dot product
+ * times both blocks' scales:
+ *   z[t][v] = inv_temp * sum_b s_h[t][b] s_W[v / 128][b] sum_{k in b} qh[t][k] qW[v][k]
+ */
+
+/* Quantise a bf16 matrix [rows][H] in blocks of block_rows x 128: codes
+ * [rows][H], scales [ceil(rows / block_rows)][ceil(H / 128)]. */
+int oracle_quantize_fp8_blocks(const uint16_t *x, int64_t rows, int64_t H, int64_t block_rows,
+                               uint8_t *codes, float *scales)
+{
+    if (!x || !codes || !scales || rows < 0 || H <= 0 || block_rows <= 0) return -1;
+    const int64_t nkb = (H + 127) / 128, nrb = (rows + block_rows - 1) / block_rows;
+#pragma omp parallel for schedule(static)
+    for (int64_t rb = 0; rb < nrb; ++rb) {
+        const int64_t r0 = rb * block_rows, r1 = r0 + block_rows < rows ? r0 + block_rows : rows;
+        for (int64_t b = 0; b < nkb; ++b) {
+            const int64_t k0 = b * 128, k1 = k0 + 128 < H ? k0 + 128 : H;
+            float amax = 0.0f;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t k = k0; k < k1; ++k) {
+                    float v = (float)bf16_to_double(x[r * H + k]);
+                    if (fabsf(v) > amax) amax = fabsf(v);
+                }
+            float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+            scales[rb * nkb + b] = sc;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t k = k0; k < k1; ++k) {
+                    float v = (float)bf16_to_double(x[r * H + k]);
+                    codes[r * H + k] = e4m3_rne(v / sc);
+                }
+        }
+    }
+    return 0;
+}
+
+/* Selected-token logprob from block-quantised operands, by definition in fp64:
+ * sh [T][ceil(H/128)], sw [ceil(V/128)][ceil(H/128)]. */
+int oracle_logprob_fp8_block(const uint8_t *qh, const float *sh, const uint8_t *qw,
+                             const float *sw, const int32_t *targets, int64_t T, int64_t H,
+                             int64_t V, float inv_temp, const int64_t *rows, int64_t n_rows,
+                             double *out_logp, double *out_lse, int64_t *out_argmax,
+                             double *out_top2gap)
+{
+    if (!qh || !sh || !qw || !sw || !targets || T < 0 || H <= 0 || V <= 0 || n_rows < 0)
+        return -1;
+    if (!rows && n_rows != T) return -1;
+    const int64_t nkb = (H + 127) / 128;
+    double lut[256];
+    for (int c = 0; c < 256; ++c) lut[c] = e4m3_value((uint8_t)c);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *z = (double *)malloc((size_t)V * sizeof(double));
+        if (!z) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_rows; ++i) {
+            if (!z) continue;
+            int64_t t = rows ? rows[i] : i;
+            if (t < 0 || t >= T) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            for (int64_t v = 0; v < V; ++v) {
+                double acc = 0.0;
+                for (int64_t b = 0; b < nkb; ++b) {
+                    const int64_t k0 = b * 128, k1 = k0 + 128 < H ? k0 + 128 : H;
+                    double part = 0.0;
+                    for (int64_t k = k0; k < k1; ++k) part += lut[qh[t * H + k]] * lut[qw[v * H + k]];
+#if ORACLE_MUTANT == 12
+                    /* mutant: the next W block row's scale (wrapping) */
+                    const double swb = (double)sw[((v / 128 + 1) % ((V + 127) / 128)) * nkb + b];
+#else
+                    const double swb = (double)sw[(v / 128) * nkb + b];
+#endif
+#if ORACLE_MUTANT == 13
+                    const double shb = (double)sh[t * nkb]; /* mutant: block 0's scale for every block */
+#else
+                    const double shb = (double)sh[t * nkb + b];
+#endif
+                    acc += shb * swb * part;
+                }
+                z[v] = acc * (double)inv_temp;
+            }
+            row_result r = logprob_row(z, V, targets[t]);
+            if (out_logp) out_logp[i] = r.logp;
+            if (out_lse) out_lse[i] = r.lse;
+            if (out_argmax) out_argmax[i] = r.argmax;
+            if (out_top2gap) out_top2gap[i] = r.top2gap;
+        }
+        free(z);
+    }
+    return bad ? -1 : 0;
+}

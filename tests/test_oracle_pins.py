@@ -451,11 +451,91 @@ def pin_fp8_logprob(lib):
     assert np.array_equal(r["argmax"], np.argmax(z, axis=1))
 
 
+def _exact_block_operand(rng, rows, H, block_rows, ints):
+    """bf16 matrix whose block_rows x 128 blocks quantise exactly: each block is
+    2^e times e4m3-representable integers, with one element 448 * 2^e, so its
+    scale amax/448 is exactly 2^e (e drawn per block) and every code is exact."""
+    x = np.zeros((rows, H), np.float32)
+    for r0 in range(0, rows, block_rows):
+        for k0 in range(0, H, 128):
+            r1, k1 = min(rows, r0 + block_rows), min(H, k0 + 128)
+            e = int(rng.integers(-12, -2))
+            blk = rng.choice(ints, (r1 - r0, k1 - k0)) * rng.choice([-1, 1], (r1 - r0, k1 - k0))
+            blk[0, 0] = 448.0
+            x[r0:r1, k0:k1] = blk * 2.0 ** e
+    return x
+
+
+def pin_fp8_block_quantiser(lib):
+    """Block e4m3 quantisation (1 x 128 and 128 x 128 blocks, ragged edges): each
+    block's scale is its amax/448 in fp32, each code torch's RNE cast of x/s."""
+    import torch
+    rng = np.random.default_rng(43)
+    x = rng.standard_normal((130, 200)).astype(np.float32)
+    x[:, 128:] *= 40.0          # a second k block with a different scale
+    x[128:, :] *= 1e-3          # a second, short row block
+    x[5, 130:140] = 0.0
+    xb = _bf16_bits_round(x)
+    xf = _bits_to_f64(xb).astype(np.float32)
+    for br in (1, 128):
+        codes, scales = oracle.quantize_fp8_blocks(xb, br, lib=lib)
+        assert scales.shape == ((130 + br - 1) // br, 2)
+        for rb in range(scales.shape[0]):
+            for b in range(2):
+                blk = xf[rb * br:(rb + 1) * br, b * 128:(b + 1) * 128]
+                amax = np.float32(np.max(np.abs(blk)))
+                s = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+                assert scales[rb, b] == s, (br, rb, b)
+                ref = torch.from_numpy((blk / s).astype(np.float32)).to(torch.float8_e4m3fn)
+                got = codes[rb * br:(rb + 1) * br, b * 128:(b + 1) * 128]
+                assert np.array_equal(got, ref.view(torch.uint8).numpy()), (br, rb, b)
+
+
+def pin_fp8_block_logprob(lib):
+    """Block-FP8 logprob: on inputs whose blocks quantise exactly (every block a
+    different power-of-two scale) it equals the bf16 oracle, which the per-row
+    fp8 oracle on the same inputs does not (the pin sees block scales); on random
+    inputs it equals scipy's log-softmax of the block-dequantised logits."""
+    rng = np.random.default_rng(44)
+    ints = np.array([0, 1, 2, 3, 4, 5, 6, 7, 8, 12, 16, 32], np.float32)
+    T, H, V = 3, 320, 300           # 3 k blocks (the last ragged), 3 W block rows (ragged)
+    hb = _bf16_bits(_exact_block_operand(rng, T, H, 1, ints))
+    wb = _bf16_bits(_exact_block_operand(rng, V, H, 128, ints))
+    tg = rng.integers(0, V, T).astype(np.int32)
+    qh, sh = oracle.quantize_fp8_blocks(hb, 1, lib=lib)
+    qw, sw = oracle.quantize_fp8_blocks(wb, 128, lib=lib)
+    assert len(np.unique(sh)) > 3 and len(np.unique(sw)) > 3   # scales differ by block
+    assert np.all(np.log2(sh) == np.round(np.log2(sh)))        # exact powers of two
+    a = oracle.logprob_fp8_block(qh, sh, qw, sw, tg, 0.5, lib=lib)
+    b = oracle.logprob(hb, wb, tg, 0.5, lib=lib)
+    for k in ("logp", "lse", "argmax"):
+        assert np.allclose(a[k], b[k], rtol=1e-12, atol=1e-12), k
+    qr, sr = oracle.quantize_fp8_rows(hb, lib=lib)
+    qv, sv = oracle.quantize_fp8_rows(wb, lib=lib)
+    c = oracle.logprob_fp8(qr, sr, qv, sv, tg, 0.5, lib=lib)
+    assert not np.allclose(c["logp"], b["logp"], rtol=1e-6, atol=1e-6)
+    tab = _e4m3_table()
+    hr = _bf16_bits_round(rng.standard_normal((4, 256)).astype(np.float32))
+    wr = _bf16_bits_round((0.05 * rng.standard_normal((260, 256))).astype(np.float32))
+    qh, sh = oracle.quantize_fp8_blocks(hr, 1, lib=lib)
+    qw, sw = oracle.quantize_fp8_blocks(wr, 128, lib=lib)
+    tg = rng.integers(0, 260, 4).astype(np.int32)
+    z = np.zeros((4, 260))
+    for bk in range(2):
+        ks = slice(bk * 128, (bk + 1) * 128)
+        z += (tab[qh[:, ks]] @ tab[qw[:, ks]].T) * sh[:, bk].astype(np.float64)[:, None] * \
+            sw[np.arange(260) // 128, bk].astype(np.float64)[None, :]
+    r = oracle.logprob_fp8_block(qh, sh, qw, sw, tg, 1.0, lib=lib)
+    assert np.allclose(r["lse"], scipy.special.logsumexp(z, axis=1), atol=1e-11)
+    assert np.allclose(r["logp"], scipy.special.log_softmax(z, axis=1)[np.arange(4), tg], atol=1e-11)
+    assert np.array_equal(r["argmax"], np.argmax(z, axis=1))
+
+
 PINS = [pin_zero_weights, pin_one_hot_dominant, pin_shift_invariance, pin_temperature,
         pin_brute_force_exact, pin_scipy_logsumexp, pin_ignored_targets,
         pin_block_stats_and_merge, pin_worked_example, pin_stats_closed_forms,
         pin_backward_finite_differences, pin_backward_closed_forms, pin_entropy,
-        pin_fp8_quantiser, pin_fp8_logprob]
+        pin_fp8_quantiser, pin_fp8_logprob, pin_fp8_block_quantiser, pin_fp8_block_logprob]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -487,7 +567,7 @@ def test_pins_catch_planted_mistakes(tmp_path):
     sign, swapped gap direction, sample variance, backward without inv_temp,
     unnormalised softmax in the backward, entropy without the LSE shift, fp8
     rounding up instead of to nearest) fails at least one pin."""
-    for mutant in range(1, 12):
+    for mutant in range(1, 14):
         path = str(tmp_path / f"liboracle_m{mutant}.so")
         oracle.build(path, mutant=mutant)
         lib = oracle.load(path)
