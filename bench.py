@@ -22,8 +22,8 @@ host buffers (H2D of h and targets, D2H of logp/lse/argmax and the 8
 statistics inside the timed region; W stays resident as model weights do), the dominant kernel's roofline from live CUDA events, SM
 clocks sampled during the timed region, the CPU oracle's throughput on a
 bounded sample, decode-regime points (T = 1..256: HBM-bound at small T), the
-backward (rlk_logprob_backward on the same batch), the FP8 (W8A8) variant, the
-entropy path and the vocabulary-sharded phases (R = 2, 3, 6 shards emulated on
+backward (rlk_logprob_backward on the same batch), the FP8 (W8A8) variants
+(per-row and block-scaled scales), the entropy path and the vocabulary-sharded phases (R = 2, 3, 6 shards emulated on
 one GPU).
 
 --workload picks the batch a step runs over: train4096 (the default above),
@@ -511,6 +511,59 @@ def fp8_points(rlk, torch, h, W, tg, pk, reps=20):
     return res
 
 
+def fp8_block_points(rlk, torch, h, W, tg, pk, reps=20):
+    """The block-scaled FP8 variant (1 x 128 activation blocks, 128 x 128 weight
+    blocks) on the same batch: weight block quantisation, the whole
+    rlk_logprob_fp8_block call at T=4096 against the fp8 tensor peak (measured
+    bf16 burst x 2), and decode calls streaming the e4m3 weight against HBM."""
+    T, H = h.shape
+    V = W.shape[0]
+    wq, wsc = rlk.quantize_fp8_weight_blocks(W)
+    stream = torch.cuda.current_stream()
+    res = {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(5):
+        rlk.quantize_fp8_weight_blocks(W, out=(wq, wsc))
+    e1.record(stream)
+    e1.synchronize()
+    tq = e0.elapsed_time(e1) / 5 * 1e-3
+    qbytes = V * H * 2 + wq.numel() + wsc.numel() * 4
+    res["quantize_weight"] = dict(ms_per_call=tq * 1e3, hbm_gbs=qbytes / tq / 1e9,
+                                  hbm_frac=qbytes / tq / 1e9 / pk["hbm_gbs"])
+
+    def timed(hh, tt, n):
+        buf = torch.empty(rlk.fp8_block_workspace_size(hh.shape[0], H, V), dtype=torch.uint8,
+                          device=h.device)
+        out = [torch.empty(hh.shape[0], device=h.device, dtype=dt)
+               for dt in (torch.float32, torch.float32, torch.int32)]
+        for _ in range(3):
+            rlk.logprob_fp8_block(hh, wq, wsc, tt, V, 1.0, workspace=buf, out=out)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            rlk.logprob_fp8_block(hh, wq, wsc, tt, V, 1.0, workspace=buf, out=out)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n * 1e-3
+
+    t = timed(h, tg, reps)
+    peak8 = 2.0 * pk["bf16_tflops"]
+    fl = 2.0 * T * H * V
+    res["forward_T4096"] = dict(tokens_per_s=T / t, ms_per_call=t * 1e3, tflops=fl / t / 1e12,
+                                peak_tflops=peak8, frac=fl / t / 1e12 / peak8,
+                                peak_note="fp8 peak = measured bf16 burst x 2 (nominal ratio)")
+    for Td in (1, 16):
+        td = timed(h[:Td].contiguous(), tg[:Td].contiguous(), 50)
+        wb = V * H + wsc.numel() * 4
+        res[f"decode_T{Td}"] = dict(tokens_per_s=Td / td, us_per_call=td * 1e6,
+                                     hbm_gbs=wb / td / 1e9, hbm_frac=wb / td / 1e9 / pk["hbm_gbs"])
+    rlk.check_device_error()
+    return res
+
+
 def run_decode_only(args):
     """Decode regime alone (T = --decode-T rows per call, H=4096, V=151936): used
     for profiling the weight-streaming regime; prints one JSON line."""
@@ -707,9 +760,10 @@ def run_ours(args):
     backward = None
     if not args.no_backward and default_wl:
         backward = backward_point(rlk, torch, h, W, tg, pk)
-    fp8 = None
+    fp8 = fp8_block = None
     if not args.no_fp8 and default_wl:
         fp8 = fp8_points(rlk, torch, h, W, tg, pk)
+        fp8_block = fp8_block_points(rlk, torch, h, W, tg, pk)
     entropy = None if (args.no_entropy or not default_wl) else entropy_point(rlk, torch, h, W, tg, pk)
     sharded = None if (args.no_shard or not default_wl) else shard_points(rlk, torch, h, W, tg, pk)
 
@@ -746,7 +800,8 @@ def run_ours(args):
                 clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"],
                             reasons=clk["reasons"], samples=clk["samples"],
                             window=clk.get("window")),
-                decode=decode, backward=backward, fp8=fp8, entropy=entropy, sharded=sharded,
+                decode=decode, backward=backward, fp8=fp8, fp8_block=fp8_block,
+                entropy=entropy, sharded=sharded,
                 bitwise_mismatch_vs_first_call=mism)
     print(json.dumps(line), flush=True)
     return 0

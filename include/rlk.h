@@ -245,6 +245,48 @@ rlk_status rlk_logprob_fp8(const void *hidden_bf16, const uint8_t *weight_e4m3,
                            size_t workspace_bytes, rlk_stream_t stream);
 
 /*
+ * Block-scaled FP8 (W8A8) variant: the block-FP8 format of DeepGEMM's W8A8
+ * batch-invariant mode, which the consistency blog uses for its dense layers
+ * ("Finish RL Training Faster: Bitwise-Consistent, High-Performance,
+ * Agent-Driven", dense-GEMM section).  The page gives no block shape for an LM
+ * head; DeepGEMM's is taken: h in 1 x 128 blocks (one token, 128 consecutive
+ * k), W in 128 x 128 blocks (128 vocabulary rows, 128 consecutive k).  Per
+ * block s = amax / 448 (fp32 IEEE division; 1 for an all-zero block), code =
+ * e4m3 RNE of x / s (fp32 division, saturating at +-448, the sign kept for a
+ * zero magnitude).  The logits:
+ *   P_b = sum_{k in block b} qh[t][k] qW[v][k]        (tensor core, fp32, per block)
+ *   acc = fma(P_b, s_h[t][b] * s_W[v/128][b], acc)     b = 0, 1, ..., H/128 - 1 in order
+ *   z   = acc * inv_temp
+ * then the same vocabulary-tile statistics and merge as rlk_logprob.  A row's
+ * results keep the batch-invariance contract (one launch shape for every T).
+ * H % 128 == 0 (else RLK_ERR_ALIGNMENT).
+ *
+ * rlk_quantize_fp8_row_blocks: h-style quantisation of x_bf16 [rows][H] into
+ *   row-major codes [rows][H] and scales [rows][H/128] f32.  Asynchronous.
+ * rlk_quantize_fp8_weight_blocks: W [V][H] into the tile-packed fp8 weight
+ *   format of rlk_quantize_fp8_weight (rlk_fp8_weight_bytes(V, H) bytes) and
+ *   scales [ceil(V/128)][H/128] f32 (rlk_fp8_block_weight_scale_count(V, H)
+ *   floats).  Asynchronous; run once per weight update.
+ * rlk_logprob_fp8_block: quantise h into the workspace, then the block-FP8
+ *   LM-head kernel and the fixed-tree merge.  weight_e4m3 / weight_scales_f32
+ *   as produced by rlk_quantize_fp8_weight_blocks; workspace >=
+ *   rlk_logprob_fp8_block_workspace_size(T, H, V), 16-byte aligned.  Other
+ *   arguments and outputs as rlk_logprob_ws.
+ */
+size_t rlk_fp8_block_weight_scale_count(int64_t V, int64_t H);
+rlk_status rlk_quantize_fp8_row_blocks(const void *x_bf16, int64_t rows, int64_t H,
+                                       uint8_t *codes, float *scales, rlk_stream_t stream);
+rlk_status rlk_quantize_fp8_weight_blocks(const void *weight_bf16, int64_t V, int64_t H,
+                                          uint8_t *packed_e4m3, float *scales,
+                                          rlk_stream_t stream);
+size_t rlk_logprob_fp8_block_workspace_size(int64_t T, int64_t H, int64_t V);
+rlk_status rlk_logprob_fp8_block(const void *hidden_bf16, const uint8_t *weight_e4m3,
+                                 const float *weight_scales_f32, const int32_t *targets_i32,
+                                 int64_t T, int64_t H, int64_t V, float inv_temp,
+                                 float *out_logp_f32, float *out_lse_f32, int32_t *out_argmax_i32,
+                                 void *workspace, size_t workspace_bytes, rlk_stream_t stream);
+
+/*
  * rlk_logprob plus the per-token entropy of the softmax over the whole
  * vocabulary, entropy[t] = -sum_v p[t][v] log p[t][v] (the actor-entropy signal
  * reported next to rewards in "Finish RL Training Faster: Bitwise-Consistent,
@@ -286,7 +328,8 @@ rlk_status rlk_logprob_entropy(const void *hidden_bf16, const void *weight_bf16,
  *   workspace      device, 16-byte aligned, >= rlk_logprob_backward_workspace_size
  *                  bytes; holds dz as bf16 [T][ldz] row-major at offset 0 on
  *                  return, ldz = rlk_logprob_backward_dz_ld(V) = V rounded up to
- *                  a multiple of 8 (the padding columns are unspecified)
+ *                  a multiple of 8 (the padding columns are unspecified); the
+ *                  rest holds the grad_h partial sums
  * Other arguments and conditions as rlk_logprob.  Asynchronous on `stream`;
  * allocates nothing.  Deterministic run to run and across GPUs of the same
  * kind; unlike the forward, the gradients are not promised to be independent

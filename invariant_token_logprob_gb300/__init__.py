@@ -21,7 +21,8 @@ __all__ = ["RlkError", "lib", "logprob", "logprob_ws", "logprob_partials", "lse_
            "logprob_backward", "backward_workspace_size", "backward_dz", "selected_token_logprob",
            "logprob_entropy", "entropy_workspace_size", "logprob_partials_shard",
            "lse_merge_sharded", "quantize_fp8_rows", "logprob_fp8", "fp8_workspace_size",
-           "quantize_fp8_weight", "unpack_fp8_weight", "consistency_stats_async",
+           "quantize_fp8_weight", "unpack_fp8_weight", "quantize_fp8_row_blocks",
+           "quantize_fp8_weight_blocks", "logprob_fp8_block", "fp8_block_workspace_size", "consistency_stats_async",
            "stats_workspace_size", "stats_dict",
            "header_functions", "STAT_NAMES", "LIB_PATH", "HEADER_PATH"]
 
@@ -106,6 +107,16 @@ def lib() -> ctypes.CDLL:
         L.rlk_logprob_fp8_workspace_size.argtypes = [i64, i64, i64]
         L.rlk_logprob_fp8.restype = st
         L.rlk_logprob_fp8.argtypes = [P, P, P, P, i64, i64, i64, f32, P, P, P, P, sz, P]
+        L.rlk_fp8_block_weight_scale_count.restype = sz
+        L.rlk_fp8_block_weight_scale_count.argtypes = [i64, i64]
+        L.rlk_quantize_fp8_row_blocks.restype = st
+        L.rlk_quantize_fp8_row_blocks.argtypes = [P, i64, i64, P, P, P]
+        L.rlk_quantize_fp8_weight_blocks.restype = st
+        L.rlk_quantize_fp8_weight_blocks.argtypes = [P, i64, i64, P, P, P]
+        L.rlk_logprob_fp8_block_workspace_size.restype = sz
+        L.rlk_logprob_fp8_block_workspace_size.argtypes = [i64, i64, i64]
+        L.rlk_logprob_fp8_block.restype = st
+        L.rlk_logprob_fp8_block.argtypes = [P, P, P, P, i64, i64, i64, f32, P, P, P, P, sz, P]
         L.rlk_logprob_entropy_workspace_size.restype = sz
         L.rlk_logprob_entropy_workspace_size.argtypes = [i64, i64, i64]
         L.rlk_logprob_entropy.restype = st
@@ -528,4 +539,68 @@ def logprob_fp8(h, W_packed, W_scales, targets, inv_temp: float = 1.0, workspace
                                  ctypes.c_float(inv_temp), _ptr(lp), _ptr(lse), _ptr(am),
                                  _ptr(workspace), workspace.numel(), _stream(stream)),
            "rlk_logprob_fp8")
+    return lp, lse, am
+
+
+def quantize_fp8_row_blocks(x, stream=None):
+    """rlk_quantize_fp8_row_blocks: bf16 [rows, H] -> (e4m3 codes uint8 [rows, H], f32
+    scales [rows, H/128]) in 1 x 128 blocks."""
+    import torch
+    _need(x, torch.bfloat16, "x", 2)
+    rows, H = x.shape
+    codes = torch.empty((rows, H), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((rows, max(1, H // 128)), dtype=torch.float32, device=x.device)
+    _check(lib().rlk_quantize_fp8_row_blocks(_ptr(x), rows, H, _ptr(codes), _ptr(scales),
+                                             _stream(stream)), "rlk_quantize_fp8_row_blocks")
+    return codes, scales
+
+
+def quantize_fp8_weight_blocks(W, out=None, stream=None):
+    """rlk_quantize_fp8_weight_blocks: bf16 W [V, H] -> (tile-packed e4m3 codes, flat
+    uint8; f32 scales [ceil(V/128), H/128]) in 128 x 128 blocks."""
+    import torch
+    _need(W, torch.bfloat16, "W", 2)
+    V, H = W.shape
+    if out is None:
+        packed = torch.empty(lib().rlk_fp8_weight_bytes(V, H), dtype=torch.uint8, device=W.device)
+        scales = torch.empty(((V + 127) // 128, max(1, H // 128)), dtype=torch.float32,
+                             device=W.device)
+    else:
+        packed, scales = out
+        _need(packed, torch.uint8, "packed", 1)
+        _need(scales, torch.float32, "scales")
+        if (packed.numel() < lib().rlk_fp8_weight_bytes(V, H) or
+                scales.numel() < lib().rlk_fp8_block_weight_scale_count(V, H)):
+            raise ValueError("out buffers too small")
+    _check(lib().rlk_quantize_fp8_weight_blocks(_ptr(W), V, H, _ptr(packed), _ptr(scales),
+                                                _stream(stream)), "rlk_quantize_fp8_weight_blocks")
+    return packed, scales
+
+
+def fp8_block_workspace_size(T: int, H: int, V: int) -> int:
+    return lib().rlk_logprob_fp8_block_workspace_size(int(T), int(H), int(V))
+
+
+def logprob_fp8_block(h, W_packed, W_scales, targets, V: int, inv_temp: float = 1.0,
+                      workspace=None, out=None, stream=None):
+    """rlk_logprob_fp8_block: (logp, lse, argmax) from bf16 h and a block-quantised
+    tile-packed e4m3 W with its [ceil(V/128), H/128] block scales."""
+    import torch
+    _need(h, torch.bfloat16, "h", 2)
+    _need(W_packed, torch.uint8, "W_packed", 1)
+    _need(W_scales, torch.float32, "W_scales")
+    _need(targets, torch.int32, "targets", 1)
+    T, H = h.shape
+    if (W_packed.numel() < lib().rlk_fp8_weight_bytes(V, H) or targets.shape[0] != T or
+            W_scales.numel() < lib().rlk_fp8_block_weight_scale_count(V, H)):
+        raise ValueError("W_packed / W_scales too small for (V, H), or targets not [T]")
+    lp, lse, am = _outputs(T, h.device, out)
+    if workspace is None:
+        workspace = torch.empty(max(1, fp8_block_workspace_size(T, H, V)), dtype=torch.uint8,
+                                device=h.device)
+    _need(workspace, torch.uint8, "workspace", 1)
+    _check(lib().rlk_logprob_fp8_block(_ptr(h), _ptr(W_packed), _ptr(W_scales), _ptr(targets), T,
+                                       H, int(V), ctypes.c_float(inv_temp), _ptr(lp), _ptr(lse),
+                                       _ptr(am), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)), "rlk_logprob_fp8_block")
     return lp, lse, am

@@ -182,6 +182,19 @@ bool encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, ui
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+bool encode_tensor_map_f32_3d(CUtensorMap* map, void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                              uint64_t stride1_bytes, uint64_t stride2_bytes) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {cuuint64_t(d0), cuuint64_t(d1), cuuint64_t(d2)};
+    const cuuint64_t strides[2] = {cuuint64_t(stride1_bytes), cuuint64_t(stride2_bytes)};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
 }  // namespace rlk
 
 extern "C" {
@@ -443,6 +456,89 @@ rlk_status rlk_logprob_fp8(const void* hidden_bf16, const uint8_t* weight_e4m3,
                                            out_argmax_i32, s));
 }
 
+size_t rlk_fp8_block_weight_scale_count(int64_t V, int64_t H) {
+    if (V <= 0 || H <= 0) return 0;
+    return size_t((V + 127) / 128) * size_t((H + 127) / 128);
+}
+
+rlk_status rlk_quantize_fp8_row_blocks(const void* x_bf16, int64_t rows, int64_t H, uint8_t* codes,
+                                       float* scales, rlk_stream_t stream) {
+    if (rows < 0 || H < 1 || H > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    if (rows == 0) return RLK_OK;
+    if (!x_bf16 || !codes || !scales) return RLK_ERR_INVALID_ARG;
+    if (H % 128 != 0 || !aligned16(x_bf16) || !aligned16(codes) || !aligned4(scales))
+        return RLK_ERR_ALIGNMENT;
+    int dev, sms;
+    rlk_status st = current_device(&dev, &sms);
+    if (st != RLK_OK) return st;
+    return from_cuda(rlk::launch_quantize_fp8_row_blocks(x_bf16, rows, rows, H, codes, scales,
+                                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rlk_status rlk_quantize_fp8_weight_blocks(const void* weight_bf16, int64_t V, int64_t H,
+                                          uint8_t* packed_e4m3, float* scales,
+                                          rlk_stream_t stream) {
+    if (V < 1 || V > INT32_MAX || H < 1 || H > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    if (!weight_bf16 || !packed_e4m3 || !scales) return RLK_ERR_INVALID_ARG;
+    if (H % 128 != 0 || !aligned16(weight_bf16) || !aligned16(packed_e4m3) || !aligned4(scales))
+        return RLK_ERR_ALIGNMENT;
+    int dev, sms;
+    rlk_status st = current_device(&dev, &sms);
+    if (st != RLK_OK) return st;
+    return from_cuda(rlk::launch_quantize_fp8_weight_blocks(weight_bf16, V, H, packed_e4m3, scales,
+                                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+int64_t fp8b_h_rows(int64_t T) {
+    const int64_t box = rlk::lmhead_fp8b_a_box_rows(T);
+    return (T + box - 1) / box * box;
+}
+}  // namespace
+
+size_t rlk_logprob_fp8_block_workspace_size(int64_t T, int64_t H, int64_t V) {
+    if (T <= 0 || V <= 0 || H <= 0) return 0;
+    const size_t rows = size_t(fp8b_h_rows(T));
+    return partial_bytes(T, V) + round16(rows * size_t(H)) +
+           round16(size_t(T) * size_t((H + 127) / 128) * 4);
+}
+
+rlk_status rlk_logprob_fp8_block(const void* hidden_bf16, const uint8_t* weight_e4m3,
+                                 const float* weight_scales_f32, const int32_t* targets_i32,
+                                 int64_t T, int64_t H, int64_t V, float inv_temp,
+                                 float* out_logp_f32, float* out_lse_f32, int32_t* out_argmax_i32,
+                                 void* workspace, size_t workspace_bytes, rlk_stream_t stream) {
+    rlk_status st = check_shape(T, H, V, inv_temp);
+    if (st != RLK_OK) return st;
+    if (T == 0) return RLK_OK;
+    if ((st = check_operands(hidden_bf16, weight_e4m3, targets_i32, H)) != RLK_OK) return st;
+    if (!weight_scales_f32) return RLK_ERR_INVALID_ARG;
+    if (H % 128 != 0 || !aligned4(weight_scales_f32)) return RLK_ERR_ALIGNMENT;
+    if ((st = check_outputs(out_logp_f32, out_lse_f32, out_argmax_i32)) != RLK_OK) return st;
+    if (!workspace) return RLK_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return RLK_ERR_ALIGNMENT;
+    if (workspace_bytes < rlk_logprob_fp8_block_workspace_size(T, H, V)) return RLK_ERR_WORKSPACE;
+    int dev, sms;
+    if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t hrows = fp8b_h_rows(T);
+    char* base = static_cast<char*>(workspace);
+    uint8_t* qh = reinterpret_cast<uint8_t*>(base + partial_bytes(T, V));
+    float* sh = reinterpret_cast<float*>(base + partial_bytes(T, V) + round16(size_t(hrows) * H));
+    cudaError_t e = rlk::launch_quantize_fp8_row_blocks(hidden_bf16, T, hrows, H, qh, sh, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    CUtensorMap th, tw;
+    const int64_t packed_rows = num_vocab_tiles(V) * (H / 128) * kVocabTile;
+    if (!encode_2d(&th, qh, hrows, H, rlk::lmhead_fp8b_a_box_rows(T), true) ||
+        !encode_2d(&tw, weight_e4m3, packed_rows, 128, kVocabTile, true))
+        return RLK_ERR_CUDA;
+    e = rlk::launch_lmhead_partials_fp8_block(&th, &tw, targets_i32, sh, weight_scales_f32,
+                                              workspace, T, V, H, inv_temp, sms, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(rlk::launch_lse_merge(workspace, targets_i32, T, V, out_logp_f32, out_lse_f32,
+                                           out_argmax_i32, s));
+}
+
 size_t rlk_logprob_entropy_workspace_size(int64_t T, int64_t H, int64_t V) {
     if (T <= 0 || V <= 0 || H <= 0) return 0;
     return partial_bytes(T, V) + (size_t(T) * size_t(num_vocab_tiles(V)) * 4 + 15) / 16 * 16;
@@ -480,6 +576,7 @@ rlk_status rlk_logprob_entropy(const void* hidden_bf16, const void* weight_bf16,
 }
 
 namespace {
+// dz [T][ldz(V)], then the K-range partial sums of grad_h
 size_t backward_dz_bytes(int64_t T, int64_t V) {
     return (size_t(T) * size_t(rlk::backward_dz_ld(V)) * 2 + 255) / 256 * 256;
 }
@@ -518,11 +615,11 @@ rlk_status rlk_logprob_backward(const void* hidden_bf16, const void* weight_bf16
     CUtensorMap th, tw;
     if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, &th, &tw)) != RLK_OK)
         return st;
+    void* split_ws = static_cast<char*>(workspace) + backward_dz_bytes(T, V);
     cudaError_t e = rlk::launch_lmhead_grad_logits(&th, &tw, targets_i32, lse_f32, grad_logp_f32,
                                                    workspace, rlk::backward_dz_ld(V), T, V, H,
                                                    inv_temp, sms, s);
     if (e != cudaSuccess) return from_cuda(e);
-    void* split_ws = static_cast<char*>(workspace) + backward_dz_bytes(T, V);
     e = rlk::run_backward_gemms(hidden_bf16, weight_bf16, workspace, T, H, V, inv_temp,
                                 grad_hidden_f32, grad_weight_f32, accumulate_grad_weight != 0,
                                 split_ws, sms, s);
@@ -615,11 +712,12 @@ rlk_status rlk_take_device_errors(rlk_stream_t stream, uint32_t* wait_error_bits
     if (st != RLK_OK) return st;
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return RLK_ERR_CUDA;
-    unsigned int word = 0, word_bwd = 0;
+    unsigned int word = 0, word_bwd = 0, word_fp8b = 0;
     unsigned long long rows = 0;
     if (rlk::lmhead_take_error(&word) != cudaSuccess) return RLK_ERR_CUDA;
     if (rlk::bwd_gemm_take_error(&word_bwd) != cudaSuccess) return RLK_ERR_CUDA;
-    word |= word_bwd;
+    if (rlk::lmhead_fp8b_take_error(&word_fp8b) != cudaSuccess) return RLK_ERR_CUDA;
+    word |= word_bwd | word_fp8b;
     if (rlk::take_target_range_rows(&rows) != cudaSuccess) return RLK_ERR_CUDA;
     if (wait_error_bits) *wait_error_bits = word;
     if (target_range_rows) *target_range_rows = rows;

@@ -28,8 +28,11 @@
 // buffered, 2 x 256 columns).  Persistent grid (pairs = co-resident clusters),
 // static round-robin over units; 3 pipeline stages of two k-blocks (64 KB).
 // Warp roles as in the LM-head kernel: TMA producer, single-thread MMA issuer,
-// four epilogue warps (one thread per row: TMEM -> registers -> alpha * acc,
-// optionally added to D, 16-byte stores).
+// four epilogue warps (one thread per row: TMEM -> registers -> alpha * acc).
+// The epilogue stages each warp's 32 x 32 block in shared memory and writes it
+// with one tiled bulk store (full 128-byte lines; scattered per-thread 16-byte
+// stores measured 2x the crossbar traffic); when adding to D it loads, adds
+// and stores from registers instead.
 //
 // Order of the sums: every output element is one accumulator, k = 0, 16, 32, ...
 // in order within its K range.  grad_W uses one range (all of K = T).  grad_h
@@ -78,8 +81,11 @@ constexpr int kEpiArrivals = 8;                    // epilogue warps of both CTA
 constexpr int kBarriers = 2 * kStages + 2 * kAccBufs + 3;
 // after the barriers: tmem slot, abort flag, odd CTA's issue count, its bytes per stage slot
 constexpr int kWords = 3 + kStages;
+// output staging: one 32 x 32 fp32 block (4 KB, 128-byte swizzled) per epilogue warp
+constexpr int kOutBlockBytes = 32 * 32 * 4;
+constexpr int kOutBytes = 4 * kOutBlockBytes;
 constexpr size_t kSmemBytes =
-    1024 + size_t(kStages) * kStageBytes + kBarriers * 8 + kWords * 4 + 16;
+    1024 + size_t(kStages) * kStageBytes + kOutBytes + kBarriers * 8 + kWords * 4 + 16;
 static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0 && kMnBoxBytes % 1024 == 0,
               "tiles 1024-B aligned");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -152,17 +158,19 @@ __device__ __forceinline__ bool wait_limit(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
-template <bool kAMn>
+template <bool kAMn, bool kBMn = true>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                    const __grid_constant__ CUtensorMap tmap_b, const Args p) {
-    constexpr uint32_t kIdesc = idesc_bf16_f32_major(2 * kUM, kUN, kAMn, true);
+                    const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_d, const Args p) {
+    constexpr uint32_t kIdesc = idesc_bf16_f32_major(2 * kUM, kUN, kAMn, kBMn);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
     uint8_t* smem = smem_raw + pad;
     const uint32_t tiles_addr = raw_addr + pad;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes);
+    uint8_t* out_stage = smem + size_t(kStages) * kStageBytes;  // [4][32 rows][128 B]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + kOutBytes);
     volatile uint32_t* words = reinterpret_cast<volatile uint32_t*>(bars + kBarriers);
     uint32_t* tmem_slot = const_cast<uint32_t*>(words);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(words + 1);
@@ -201,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmap_a);
         tma_prefetch_desc(&tmap_b);
+        tma_prefetch_desc(&tmap_d);
     }
     if (warp == 1) {
         tmem_alloc<2>(smem_u32(tmem_slot), kTmemCols);
@@ -271,9 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                         if (load_b) {
-                            tma_load_2d_pair(&tmap_b, fb, b_tile(stage, j), b0, kb * kBK);
-                            tma_load_2d_pair(&tmap_b, fb, b_tile(stage, j) + kMnBoxBytes,
-                                             b0 + kMnAtom, kb * kBK);
+                            if constexpr (kBMn) {
+                                tma_load_2d_pair(&tmap_b, fb, b_tile(stage, j), b0, kb * kBK);
+                                tma_load_2d_pair(&tmap_b, fb, b_tile(stage, j) + kMnBoxBytes,
+                                                 b0 + kMnAtom, kb * kBK);
+                            } else {
+                                tma_load_2d_pair(&tmap_b, fb, b_tile(stage, j), kb * kBK, b0);
+                            }
                         }
                     }
                     ++issued;
@@ -349,9 +362,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             else
                                 a_desc = sw128_kmajor_desc(a_tile(stage, j)) +
                                          uint64_t((kk * 32) >> 4);
-                            const uint64_t b_desc =
-                                sw128_mnmajor_desc(b_tile(stage, j) + kk * 2 * kKAtomBytes,
-                                                   kMnBoxBytes, kKAtomBytes);
+                            uint64_t b_desc;
+                            if constexpr (kBMn)
+                                b_desc = sw128_mnmajor_desc(b_tile(stage, j) + kk * 2 * kKAtomBytes,
+                                                            kMnBoxBytes, kKAtomBytes);
+                            else
+                                b_desc = sw128_kmajor_desc(b_tile(stage, j)) +
+                                         uint64_t((kk * 32) >> 4);
                             umma_bf16<2>(d_tmem, a_desc, b_desc, kIdesc,
                                          (kb0 + j > kb_begin || kk != 0) ? 1u : 0u);
                         }
@@ -381,6 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16);
         const float alpha = p.alpha;
+        // This warp's staging block: its 32 rows x 32 columns of one chunk,
+        // written in the 128-byte-swizzled layout the tensor store reads
+        // (16-byte piece i of row r at piece i ^ (r % 8)), which also keeps
+        // the 8 lanes of each store phase on distinct banks.
+        uint8_t* out_row = out_stage + q * kOutBlockBytes + lane * 128;
+        const uint32_t out_block = smem_u32(out_stage + q * kOutBlockBytes);
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = slot; tile < p.num_tiles; tile += nslots) {
             int s, mu, n;
@@ -396,11 +419,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ncols = min(kUN, p.N - col0);
             float* drow = p.d + int64_t(s) * p.split_stride + (live ? row : 0) * p.ldd + col0;
             const uint32_t t_addr = lane_base + acc * uint32_t(kUN);
+            const int row0 = (2 * mu + int(rank)) * kUM + q * 32;  // this warp's first row
             for (int c = 0; c * 32 < ncols; ++c) {
                 uint32_t r[32];
                 tmem_ld32(t_addr + uint32_t(c * 32), r);
                 tmem_ld_wait();
-                if (live) {
+                if (!p.accumulate) {
+                    // stage the 32 x 32 block, then one tiled bulk store (clipped
+                    // at M and N); the previous store must be done reading first
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<float4*>(out_row + ((i ^ (lane & 7)) << 4)) =
+                            make_float4(__fmul_rn(alpha, __uint_as_float(r[4 * i])),
+                                        __fmul_rn(alpha, __uint_as_float(r[4 * i + 1])),
+                                        __fmul_rn(alpha, __uint_as_float(r[4 * i + 2])),
+                                        __fmul_rn(alpha, __uint_as_float(r[4 * i + 3])));
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0 && row0 < p.M) {
+                        tma_store_3d(&tmap_d, out_block, col0 + c * 32, row0, s);
+                        bulk_commit_group();
+                    }
+                } else if (live) {
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4) {
                         if (c * 32 + q4 * 4 < ncols) {  // N % 4 == 0: quads are whole
@@ -431,6 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) bulk_wait_group<0>();  // every store of this warp has completed
+        __syncwarp();
     }
 
     tc_fence_before_sync();
@@ -466,12 +510,19 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-int g_max_clusters[2][64];  // co-resident CTA pairs per kernel variant and device
+int g_max_clusters[4][64];  // co-resident CTA pairs per kernel variant and device
 
-template <bool kAMn>
+template <bool kAMn, bool kBMn = true>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, Args a, int num_sms,
                         cudaStream_t stream) {
-    auto kernel = bwd_gemm_kernel<kAMn>;
+    // D as [S][M][ldd] fp32, stored in 32 x 32 blocks
+    CUtensorMap td;
+    const int64_t splits = (a.num_kb + a.kb_per_split - 1) / a.kb_per_split;
+    if (!encode_tensor_map_f32_3d(&td, a.d, uint64_t(a.N), uint64_t(a.M), uint64_t(splits),
+                                  uint64_t(a.ldd) * 4,
+                                  uint64_t(a.split_stride ? a.split_stride : a.M * a.ldd) * 4))
+        return cudaErrorInvalidValue;
+    auto kernel = bwd_gemm_kernel<kAMn, kBMn>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -489,7 +540,7 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, Args a, in
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    int& maxc = g_max_clusters[kAMn ? 1 : 0][dev];
+    int& maxc = g_max_clusters[(kAMn ? 1 : 0) + (kBMn ? 2 : 0)][dev];
     if (maxc == 0) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(kSmemBytes));
@@ -506,7 +557,7 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, Args a, in
     const int clusters = a.num_tiles < maxc ? a.num_tiles : maxc;
     if (clusters < 1) return cudaSuccess;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, a);
+    e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, td, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

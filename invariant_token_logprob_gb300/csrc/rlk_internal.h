@@ -34,6 +34,11 @@ int lmhead_a_box_rows(int64_t T);
 bool encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                           uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool bytes);
 
+// 3-D TMA tensor map of fp32 [d2][d1][d0] (d0 contiguous), 128-byte swizzle,
+// boxes of 32 x 32 x 1 elements: the output side of tiled bulk stores.
+bool encode_tensor_map_f32_3d(CUtensorMap* map, void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                              uint64_t stride1_bytes, uint64_t stride2_bytes);
+
 // The smallest h box the LM-head kernel copies (rows); see lmhead_a_box_rows.
 constexpr int kMinTmaRows = 16;
 
@@ -105,6 +110,27 @@ cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_ro
 // scales [V].
 cudaError_t launch_quantize_fp8_weight_tiled(const void* W, int64_t V, int64_t H, void* packed,
                                              float* scales, cudaStream_t stream);
+
+// Block-scaled FP8 (1 x 128 activation blocks, 128 x 128 weight blocks).
+// Activations: codes [out_rows][H] row-major (rows >= `rows` zero), scales
+// [rows][H/128].  Weights: the tile-packed fp8 weight format, scales
+// [ceil(V/128)][H/128].  H % 128 == 0.
+cudaError_t launch_quantize_fp8_row_blocks(const void* x, int64_t rows, int64_t out_rows, int64_t H,
+                                           void* codes, float* scales, cudaStream_t stream);
+cudaError_t launch_quantize_fp8_weight_blocks(const void* W, int64_t V, int64_t H, void* packed,
+                                              float* scales, cudaStream_t stream);
+// Rows of each h box of the block-FP8 LM-head kernel (one launch shape for
+// every T): the call's rows rounded up to 16, at most 128.
+int lmhead_fp8b_a_box_rows(int64_t T);
+// The block-FP8 LM-head kernel: th maps the h codes [h_rows][H] with boxes
+// {128, lmhead_fp8b_a_box_rows(T)}, tw the tile-packed weight as rows of 128
+// bytes with boxes {128, kVocabTile}; sh [T][H/128], sw [ceil(V/128)][H/128].
+cudaError_t launch_lmhead_partials_fp8_block(const CUtensorMap* th, const CUtensorMap* tw,
+                                             const int32_t* targets, const float* sh,
+                                             const float* sw, void* partials, int64_t T,
+                                             int64_t V, int64_t H, float inv_temp, int num_sms,
+                                             cudaStream_t stream);
+cudaError_t lmhead_fp8b_take_error(unsigned int* out);
 
 // Bounded-wait self-test of the forward kernel (single CTA for T <= 128, CTA
 // pair above): mode 1, its producer issues no copies, so the MMA warp's wait

@@ -148,6 +148,214 @@ __global__ void __launch_bounds__(kQuantThreads)
     if (t == 0) scales[r] = sc;
 }
 
+// The weight quantiser with the row held in registers: one warp per row, lane l
+// loading the 16-element groups l, l + 32, ... of the row once (up to kGroups
+// of them, H <= kGroups * 512), so each element is read from memory once; the
+// max, the scale and the conversion are those of quantize_rows_kernel, so the
+// codes and scales are bit-identical to its output.
+template <int kGroups>
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_weight_cached_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
+                                  int64_t out_rows, int H, uint8_t* __restrict__ codes,
+                                  float* __restrict__ scales) {
+    grid_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t r = int64_t(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
+    if (r >= out_rows) return;  // uniform per warp
+    if (r >= rows) {            // zero padding rows of the last vocabulary tile
+        for (int k = lane * 16; k < H; k += 32 * 16)
+            *reinterpret_cast<uint4*>(codes + code_offset<true>(r, k, H)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    const __nv_bfloat16* xr = x + r * int64_t(H);
+    uint4 v[kGroups][2];
+    float amax = 0.0f;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+        const int k = lane * 16 + g * 32 * 16;
+        if (k < H) {
+            v[g][0] = *reinterpret_cast<const uint4*>(xr + k);
+            v[g][1] = *reinterpret_cast<const uint4*>(xr + k + 8);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+        const int k = lane * 16 + g * 32 * 16;
+        if (k < H) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[g][half]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __bfloat1622float2(p[i]);
+                    amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const bool fast = sc >= 0x1p-64f;  // as quantize_rows_kernel: IEEE division below
+    const float rs = fast ? __frcp_rn(sc) : 0.0f;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+        const int k = lane * 16 + g * 32 * 16;
+        if (k < H) {
+            uint32_t out[4];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[g][half]);
+                const float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
+                const float2 c = __bfloat1622float2(p[2]), d = __bfloat1622float2(p[3]);
+                if (fast) {
+                    out[half * 2] = e4m3x4<true>(a.x, a.y, b.x, b.y, sc, rs);
+                    out[half * 2 + 1] = e4m3x4<true>(c.x, c.y, d.x, d.y, sc, rs);
+                } else {
+                    out[half * 2] = e4m3x4<false>(a.x, a.y, b.x, b.y, sc, rs);
+                    out[half * 2 + 1] = e4m3x4<false>(c.x, c.y, d.x, d.y, sc, rs);
+                }
+            }
+            *reinterpret_cast<uint4*>(codes + code_offset<true>(r, k, H)) =
+                make_uint4(out[0], out[1], out[2], out[3]);
+        }
+    }
+    if (lane == 0) scales[r] = sc;
+}
+
+constexpr int kCachedGroups = 12;  // rows of up to 12 * 512 = 6144 elements stay in registers
+
+// Block-scaled quantisation (the 1 x 128 / 128 x 128 block-FP8 format): the
+// same scale (amax / 448, IEEE division; 1 for an all-zero block) and the same
+// per-element division and RNE conversion as above, with the amax taken over
+// one block instead of one row.
+
+// Activations, 1 x 128 blocks: one warp per row, lane l converting the 16
+// elements l * 16 + g * 512 of step g; the 8 lanes of a 128-element block meet
+// in a 3-step shuffle max.  codes [out_rows][H] row-major, scales [rows][H/128];
+// rows >= `rows` (zero padding to whole h boxes) get zero codes.
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_row_blocks_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
+                               int64_t out_rows, int H, uint8_t* __restrict__ codes,
+                               float* __restrict__ scales) {
+    grid_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t r = int64_t(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
+    if (r >= out_rows) return;  // uniform per warp
+    const int nkb = H / 128;
+    for (int k = lane * 16; k < H; k += 32 * 16) {  // H % 128 == 0: whole blocks per step
+        if (r >= rows) {
+            *reinterpret_cast<uint4*>(codes + r * int64_t(H) + k) = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+        }
+        const __nv_bfloat16* xr = x + r * int64_t(H) + k;
+        const uint4 v0 = *reinterpret_cast<const uint4*>(xr);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(xr + 8);
+        float amax = 0.0f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const __nv_bfloat162* p =
+                reinterpret_cast<const __nv_bfloat162*>(half ? &v1 : &v0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(p[i]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+#pragma unroll
+        for (int off = 4; off >= 1; off >>= 1)  // the 8 lanes of this 128-element block
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        const bool fast = sc >= 0x1p-64f;
+        const float rs = fast ? __frcp_rn(sc) : 0.0f;
+        uint32_t out[4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(half ? &v1 : &v0);
+            const float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
+            const float2 c = __bfloat1622float2(p[2]), d = __bfloat1622float2(p[3]);
+            if (fast) {
+                out[half * 2] = e4m3x4<true>(a.x, a.y, b.x, b.y, sc, rs);
+                out[half * 2 + 1] = e4m3x4<true>(c.x, c.y, d.x, d.y, sc, rs);
+            } else {
+                out[half * 2] = e4m3x4<false>(a.x, a.y, b.x, b.y, sc, rs);
+                out[half * 2 + 1] = e4m3x4<false>(c.x, c.y, d.x, d.y, sc, rs);
+            }
+        }
+        *reinterpret_cast<uint4*>(codes + r * int64_t(H) + k) =
+            make_uint4(out[0], out[1], out[2], out[3]);
+        if ((lane & 7) == 0) scales[r * nkb + k / 128] = sc;
+    }
+}
+
+// Weights, 128 x 128 blocks, written in the tile-packed fp8 weight format: one
+// CTA per (block row vb, k block kb); thread t holds 64 elements of row
+// t / 2 (half t % 2 of its 128) in registers; the block's max meets through
+// warp shuffles and shared memory.  Block rows past V (padding of the last
+// 256-row vocabulary tile) get zero codes and no scale.
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_weight_blocks_kernel(const __nv_bfloat16* __restrict__ W, int64_t V, int H,
+                                  uint8_t* __restrict__ packed, float* __restrict__ scales) {
+    grid_launch_dependents();
+    const int kb = blockIdx.x;
+    const int64_t vb = blockIdx.y;
+    const int nkb = H / 128;
+    const int t = threadIdx.x;
+    const int64_t row = vb * 128 + t / 2;
+    const int col = kb * 128 + (t & 1) * 64;
+    uint4 v[8];
+    float amax = 0.0f;
+    const bool live = row < V;
+    if (live) {
+        const __nv_bfloat16* src = W + row * int64_t(H) + col;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint4*>(src + 8 * i);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __bfloat1622float2(p[j]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    __shared__ float warp_max[kQuantThreads / 32];
+    if ((t & 31) == 0) warp_max[t >> 5] = amax;
+    __syncthreads();
+    amax = warp_max[0];
+#pragma unroll
+    for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+    const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const bool fast = sc >= 0x1p-64f;
+    const float rs = fast ? __frcp_rn(sc) : 0.0f;
+    uint32_t out[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (!live) {
+            out[2 * i] = out[2 * i + 1] = 0u;
+            continue;
+        }
+        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+        const float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
+        const float2 c = __bfloat1622float2(p[2]), d = __bfloat1622float2(p[3]);
+        if (fast) {
+            out[2 * i] = e4m3x4<true>(a.x, a.y, b.x, b.y, sc, rs);
+            out[2 * i + 1] = e4m3x4<true>(c.x, c.y, d.x, d.y, sc, rs);
+        } else {
+            out[2 * i] = e4m3x4<false>(a.x, a.y, b.x, b.y, sc, rs);
+            out[2 * i + 1] = e4m3x4<false>(c.x, c.y, d.x, d.y, sc, rs);
+        }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(packed + code_offset<true>(row, col, H));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
+    if (t == 0 && vb * 128 < V) scales[vb * nkb + kb] = sc;
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_rows, int64_t H,
@@ -164,9 +372,34 @@ cudaError_t launch_quantize_fp8_weight_tiled(const void* W, int64_t V, int64_t H
     const int64_t padded = (V + kVocabTile - 1) / kVocabTile * kVocabTile;
     constexpr int kRowsPerCta = kQuantThreads / 32;  // one warp per row
     const int64_t ctas = (padded + kRowsPerCta - 1) / kRowsPerCta;
+    if (H <= int64_t(kCachedGroups) * 512) {
+        quantize_weight_cached_kernel<kCachedGroups><<<unsigned(ctas), kQuantThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(W), V, padded, int(H), static_cast<uint8_t*>(packed),
+            scales);
+        return cudaGetLastError();
+    }
     quantize_rows_kernel<true, 32><<<unsigned(ctas), kQuantThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(W), V, padded, int(H), static_cast<uint8_t*>(packed),
         scales, V);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp8_row_blocks(const void* x, int64_t rows, int64_t out_rows, int64_t H,
+                                           void* codes, float* scales, cudaStream_t stream) {
+    constexpr int kRowsPerCta = kQuantThreads / 32;  // one warp per row
+    const int64_t ctas = (out_rows + kRowsPerCta - 1) / kRowsPerCta;
+    quantize_row_blocks_kernel<<<unsigned(ctas), kQuantThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, out_rows, int(H), static_cast<uint8_t*>(codes),
+        scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp8_weight_blocks(const void* W, int64_t V, int64_t H, void* packed,
+                                              float* scales, cudaStream_t stream) {
+    const int64_t padded = (V + kVocabTile - 1) / kVocabTile * kVocabTile;
+    const dim3 grid(unsigned(H / 128), unsigned(padded / 128), 1);
+    quantize_weight_blocks_kernel<<<grid, kQuantThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(W), V, int(H), static_cast<uint8_t*>(packed), scales);
     return cudaGetLastError();
 }
 

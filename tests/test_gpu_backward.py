@@ -99,6 +99,12 @@ def test_gemms_match_fp64_products_of_the_kernels_dz(T, H, V, it):
     ref_W = base.double().cpu() + t * (dz64.T @ h64)
     bound_W = 2.0 ** -13 * (base.double().cpu().abs() + t * (dz64.abs().T @ h64.abs())) + 1e-30
     assert torch.all((gW.double().cpu() - ref_W).abs() <= bound_W), "grad_W (accumulated)"
+    # overwritten (the tiled-store path of the epilogue), and grad_h unchanged by it
+    gh2, gW2, dz2 = _run(d, grad, it)
+    assert torch.equal(dz2.view(torch.int16), dz.view(torch.int16)) and torch.equal(gh2, gh)
+    ref_W2 = t * (dz64.T @ h64)
+    bound_W2 = 2.0 ** -13 * t * (dz64.abs().T @ h64.abs()) + 1e-30
+    assert torch.all((gW2.double().cpu() - ref_W2).abs() <= bound_W2), "grad_W (overwritten)"
 
 
 def test_backward_accumulates_and_skips():
