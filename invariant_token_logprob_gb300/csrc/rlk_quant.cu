@@ -148,44 +148,70 @@ __global__ void __launch_bounds__(kQuantThreads)
     if (t == 0) scales[r] = sc;
 }
 
-// The weight quantiser with the row held in registers: one warp per row, lane l
-// loading the 16-element groups l, l + 32, ... of the row once (up to kGroups
-// of them, H <= kGroups * 512), so each element is read from memory once; the
-// max, the scale and the conversion are those of quantize_rows_kernel, so the
-// codes and scales are bit-identical to its output.
-template <int kGroups>
-__global__ void __launch_bounds__(kQuantThreads)
-    quantize_weight_cached_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
+// The weight quantiser with each row read from memory once: one warp per row,
+// the row staged in the warp's shared memory by one bulk copy, then the max
+// and the conversion of quantize_rows_kernel read it from there (same scale,
+// same division, same conversion: bit-identical codes and scales).  28 warps
+// per CTA, one 8 KB row buffer each, so many rows are in flight per SM.
+// Waits are bounded; a row whose copy never lands is skipped and recorded in
+// g_quant_error.
+constexpr int kStagedWarps = 28;
+constexpr uint64_t kQuantWaitNs = 2000000000ull;
+
+__device__ unsigned int g_quant_error;
+
+__global__ void __launch_bounds__(kStagedWarps * 32, 1)
+    quantize_weight_staged_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
                                   int64_t out_rows, int H, uint8_t* __restrict__ codes,
                                   float* __restrict__ scales) {
+    extern __shared__ __align__(16) uint8_t qsmem[];
     grid_launch_dependents();
+    const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t r = int64_t(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
-    if (r >= out_rows) return;  // uniform per warp
-    if (r >= rows) {            // zero padding rows of the last vocabulary tile
-        for (int k = lane * 16; k < H; k += 32 * 16)
-            *reinterpret_cast<uint4*>(codes + code_offset<true>(r, k, H)) =
-                make_uint4(0u, 0u, 0u, 0u);
-        return;
+    const uint32_t row_bytes = uint32_t(H) * 2;
+    uint8_t* mine = qsmem + size_t(warp) * row_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(qsmem + size_t(kStagedWarps) * row_bytes);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStagedWarps; ++i) mbar_init(smem_u32(bars + i), 1);
+        fence_mbar_init();
     }
-    const __nv_bfloat16* xr = x + r * int64_t(H);
-    uint4 v[kGroups][2];
-    float amax = 0.0f;
-#pragma unroll
-    for (int g = 0; g < kGroups; ++g) {
-        const int k = lane * 16 + g * 32 * 16;
-        if (k < H) {
-            v[g][0] = *reinterpret_cast<const uint4*>(xr + k);
-            v[g][1] = *reinterpret_cast<const uint4*>(xr + k + 8);
+    __syncthreads();
+    const uint32_t bar = smem_u32(bars + warp);
+    const int64_t stride = int64_t(gridDim.x) * kStagedWarps;
+    uint32_t phase = 0;
+    for (int64_t r = int64_t(blockIdx.x) * kStagedWarps + warp; r < out_rows; r += stride) {
+        if (r >= rows) {  // zero padding rows of the last vocabulary tile
+            for (int k = lane * 16; k < H; k += 32 * 16)
+                *reinterpret_cast<uint4*>(codes + code_offset<true>(r, k, H)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            continue;
         }
-    }
-#pragma unroll
-    for (int g = 0; g < kGroups; ++g) {
-        const int k = lane * 16 + g * 32 * 16;
-        if (k < H) {
+        if (lane == 0) {
+            fence_proxy_async_shared();  // the previous row's reads of the buffer come first
+            mbar_arrive_expect_tx(bar, row_bytes);
+            bulk_load(smem_u32(mine), x + r * int64_t(H), row_bytes, bar);
+        }
+        const uint64_t t0 = global_timer_ns();
+        bool landed = true;
+        while (!mbar_try_wait(bar, phase)) {
+            if (global_timer_ns() - t0 > kQuantWaitNs) {
+                landed = false;
+                break;
+            }
+        }
+        landed = __all_sync(0xffffffffu, landed);
+        phase ^= 1u;
+        if (!landed) {
+            if (lane == 0) atomicOr(&g_quant_error, 1u);
+            break;  // the copy may still land: this warp stops using its buffer
+        }
+        const __nv_bfloat16* xr = reinterpret_cast<const __nv_bfloat16*>(mine);
+        float amax = 0.0f;
+        for (int k = lane * 16; k < H; k += 32 * 16) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[g][half]);
+                const uint4 v = *reinterpret_cast<const uint4*>(xr + k + half * 8);
+                const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float2 f = __bfloat1622float2(p[i]);
@@ -193,38 +219,18 @@ __global__ void __launch_bounds__(kQuantThreads)
                 }
             }
         }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        if (sc >= 0x1p-64f)
+            convert_row<true, true, 32>(xr, r, H, lane, sc, __frcp_rn(sc), codes);
+        else
+            convert_row<true, false, 32>(xr, r, H, lane, sc, 0.0f, codes);
+        if (lane == 0) scales[r] = sc;
+        __syncwarp();  // every lane is done with the buffer before it is refilled
     }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    const bool fast = sc >= 0x1p-64f;  // as quantize_rows_kernel: IEEE division below
-    const float rs = fast ? __frcp_rn(sc) : 0.0f;
-#pragma unroll
-    for (int g = 0; g < kGroups; ++g) {
-        const int k = lane * 16 + g * 32 * 16;
-        if (k < H) {
-            uint32_t out[4];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[g][half]);
-                const float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
-                const float2 c = __bfloat1622float2(p[2]), d = __bfloat1622float2(p[3]);
-                if (fast) {
-                    out[half * 2] = e4m3x4<true>(a.x, a.y, b.x, b.y, sc, rs);
-                    out[half * 2 + 1] = e4m3x4<true>(c.x, c.y, d.x, d.y, sc, rs);
-                } else {
-                    out[half * 2] = e4m3x4<false>(a.x, a.y, b.x, b.y, sc, rs);
-                    out[half * 2 + 1] = e4m3x4<false>(c.x, c.y, d.x, d.y, sc, rs);
-                }
-            }
-            *reinterpret_cast<uint4*>(codes + code_offset<true>(r, k, H)) =
-                make_uint4(out[0], out[1], out[2], out[3]);
-        }
-    }
-    if (lane == 0) scales[r] = sc;
 }
-
-constexpr int kCachedGroups = 12;  // rows of up to 12 * 512 = 6144 elements stay in registers
 
 // Block-scaled quantisation (the 1 x 128 / 128 x 128 block-FP8 format): the
 // same scale (amax / 448, IEEE division; 1 for an all-zero block) and the same
@@ -372,8 +378,27 @@ cudaError_t launch_quantize_fp8_weight_tiled(const void* W, int64_t V, int64_t H
     const int64_t padded = (V + kVocabTile - 1) / kVocabTile * kVocabTile;
     constexpr int kRowsPerCta = kQuantThreads / 32;  // one warp per row
     const int64_t ctas = (padded + kRowsPerCta - 1) / kRowsPerCta;
-    if (H <= int64_t(kCachedGroups) * 512) {
-        quantize_weight_cached_kernel<kCachedGroups><<<unsigned(ctas), kQuantThreads, 0, stream>>>(
+    // rows of up to 8 KB staged once per warp in shared memory (<= 224 KB per CTA)
+    const size_t staged = size_t(kStagedWarps) * size_t(H) * 2 + kStagedWarps * 8;
+    if (H * 2 <= 8192) {
+        static int configured[64];
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64 && !configured[dev]) {
+            e = cudaFuncSetAttribute(quantize_weight_staged_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     int(kStagedWarps * 8192 + kStagedWarps * 8));
+            if (e != cudaSuccess) return e;
+            configured[dev] = 1;
+        }
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        const int64_t warps_needed = padded;
+        int64_t grid = (warps_needed + kStagedWarps - 1) / kStagedWarps;
+        if (grid > sms) grid = sms;  // persistent: one CTA per SM
+        quantize_weight_staged_kernel<<<unsigned(grid), kStagedWarps * 32, staged, stream>>>(
             static_cast<const __nv_bfloat16*>(W), V, padded, int(H), static_cast<uint8_t*>(packed),
             scales);
         return cudaGetLastError();
@@ -401,6 +426,15 @@ cudaError_t launch_quantize_fp8_weight_blocks(const void* W, int64_t V, int64_t 
     quantize_weight_blocks_kernel<<<grid, kQuantThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(W), V, int(H), static_cast<uint8_t*>(packed), scales);
     return cudaGetLastError();
+}
+
+cudaError_t quant_take_error(unsigned int* out) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_quant_error, sizeof v);
+    if (e != cudaSuccess) return e;
+    if (v) e = cudaMemcpyToSymbol(g_quant_error, &zero, sizeof zero);
+    *out = v;
+    return e;
 }
 
 }  // namespace rlk

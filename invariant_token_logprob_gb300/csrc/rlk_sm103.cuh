@@ -143,6 +143,17 @@ __device__ __forceinline__ void tma_load_2d(const void* desc, uint32_t bar, uint
         : "memory");
 }
 
+// Untiled bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completion signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // CTA-pair form: the copy lands in this CTA's shared memory and its bytes are
 // signalled on `bar_cluster`, an mbarrier of either CTA of the pair (a
 // shared::cluster address, e.g. from mapa).
