@@ -329,7 +329,9 @@ rlk_status rlk_logprob_entropy(const void *hidden_bf16, const void *weight_bf16,
  *                  bytes; holds dz as bf16 [T][ldz] row-major at offset 0 on
  *                  return, ldz = rlk_logprob_backward_dz_ld(V) = V rounded up to
  *                  a multiple of 8 (the padding columns are unspecified); the
- *                  rest holds the grad_h partial sums
+ *                  rest holds a transposed copy of dz (written only when
+ *                  grad_weight_f32 is given: the grad_W product reads it with k
+ *                  contiguous) and the grad_h partial sums
  * Other arguments and conditions as rlk_logprob.  Asynchronous on `stream`;
  * allocates nothing.  Deterministic run to run and across GPUs of the same
  * kind; unlike the forward, the gradients are not promised to be independent

@@ -182,6 +182,20 @@ bool encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, ui
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+bool encode_tensor_map_2d_store(CUtensorMap* map, void* base, uint64_t inner, uint64_t outer,
+                                uint64_t row_bytes) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+    const cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_tensor_map_f32_3d(CUtensorMap* map, void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                               uint64_t stride1_bytes, uint64_t stride2_bytes) {
     EncodeTiledFn enc = encode_fn();
@@ -576,7 +590,7 @@ rlk_status rlk_logprob_entropy(const void* hidden_bf16, const void* weight_bf16,
 }
 
 namespace {
-// dz [T][ldz(V)], then the K-range partial sums of grad_h
+// dz [T][ldz(V)], its transpose [V][ldz(T)], then the K-range partial sums of grad_h
 size_t backward_dz_bytes(int64_t T, int64_t V) {
     return (size_t(T) * size_t(rlk::backward_dz_ld(V)) * 2 + 255) / 256 * 256;
 }
@@ -584,7 +598,7 @@ size_t backward_dz_bytes(int64_t T, int64_t V) {
 
 size_t rlk_logprob_backward_workspace_size(int64_t T, int64_t H, int64_t V) {
     if (T <= 0 || V <= 0 || H <= 0) return 0;
-    return backward_dz_bytes(T, V) + rlk::backward_split_bytes(T, H, V);
+    return backward_dz_bytes(T, V) + backward_dz_bytes(V, T) + rlk::backward_split_bytes(T, H, V);
 }
 
 size_t rlk_logprob_backward_dz_ld(int64_t V) {
@@ -615,12 +629,15 @@ rlk_status rlk_logprob_backward(const void* hidden_bf16, const void* weight_bf16
     CUtensorMap th, tw;
     if ((st = prepare_maps(hidden_bf16, weight_bf16, T, H, V, &th, &tw)) != RLK_OK)
         return st;
-    void* split_ws = static_cast<char*>(workspace) + backward_dz_bytes(T, V);
-    cudaError_t e = rlk::launch_lmhead_grad_logits(&th, &tw, targets_i32, lse_f32, grad_logp_f32,
-                                                   workspace, rlk::backward_dz_ld(V), T, V, H,
-                                                   inv_temp, sms, s);
+    char* dzt = static_cast<char*>(workspace) + backward_dz_bytes(T, V);
+    void* split_ws = dzt + backward_dz_bytes(V, T);
+    CUtensorMap tdzt;
+    if (grad_weight_f32 && !rlk::encode_dzt_store_map(&tdzt, dzt, T, V)) return RLK_ERR_CUDA;
+    cudaError_t e = rlk::launch_lmhead_grad_logits(
+        &th, &tw, grad_weight_f32 ? &tdzt : nullptr, targets_i32, lse_f32, grad_logp_f32,
+        workspace, rlk::backward_dz_ld(V), T, V, H, inv_temp, sms, s);
     if (e != cudaSuccess) return from_cuda(e);
-    e = rlk::run_backward_gemms(hidden_bf16, weight_bf16, workspace, T, H, V, inv_temp,
+    e = rlk::run_backward_gemms(hidden_bf16, weight_bf16, workspace, dzt, T, H, V, inv_temp,
                                 grad_hidden_f32, grad_weight_f32, accumulate_grad_weight != 0,
                                 split_ws, sms, s);
     return from_cuda(e);

@@ -596,16 +596,23 @@ size_t backward_split_bytes(int64_t T, int64_t H, int64_t V) {
     return S > 1 ? size_t(S) * size_t(T) * size_t(H) * 4 : 0;
 }
 
-cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, int64_t T, int64_t H,
-                               int64_t V, float inv_temp, float* grad_h, float* grad_W,
-                               bool accumulate_W, void* split_ws, int num_sms,
+bool encode_dzt_store_map(CUtensorMap* map, void* dzt, int64_t T, int64_t V) {
+    return encode_tensor_map_2d_store(map, dzt, uint64_t(T), uint64_t(V),
+                                      uint64_t(backward_dz_ld(T)) * 2);
+}
+
+cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, const void* dzt,
+                               int64_t T, int64_t H, int64_t V, float inv_temp, float* grad_h,
+                               float* grad_W, bool accumulate_W, void* split_ws, int num_sms,
                                cudaStream_t stream) {
     const int64_t ldz = backward_dz_ld(V);
     if (grad_W) {
-        // grad_W [V][H] (+)= inv_temp * dz^T . h: A = dz read MN-major, B = h.
+        // grad_W [V][H] (+)= inv_temp * dz^T . h: A = dzt [V][T] read K-major (dz
+        // read in place would be an MN-major A, measured ~8% slower), B = h.
+        if (!dzt) return cudaErrorInvalidValue;
         CUtensorMap ta, tb;
-        if (!encode_tensor_map_2d(&ta, dz, uint64_t(V), uint64_t(T), uint64_t(ldz) * 2, kMnAtom,
-                                  kBK, false) ||
+        if (!encode_tensor_map_2d(&ta, dzt, uint64_t(T), uint64_t(V),
+                                  uint64_t(backward_dz_ld(T)) * 2, kBK, kUM, false) ||
             !encode_tensor_map_2d(&tb, h, uint64_t(H), uint64_t(T), uint64_t(H) * 2, kMnAtom, kBK,
                                   false))
             return cudaErrorInvalidValue;
@@ -622,7 +629,7 @@ cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, int
         a.num_tiles = a.num_mu * a.num_n;
         a.alpha = inv_temp;
         a.accumulate = accumulate_W ? 1 : 0;
-        cudaError_t e = launch_gemm<true>(ta, tb, a, num_sms, stream);
+        cudaError_t e = launch_gemm<false>(ta, tb, a, num_sms, stream);
         if (e != cudaSuccess) return e;
     }
     if (grad_h) {

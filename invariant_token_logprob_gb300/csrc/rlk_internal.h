@@ -34,6 +34,11 @@ int lmhead_a_box_rows(int64_t T);
 bool encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                           uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool bytes);
 
+// 2-D TMA tensor map of bf16 [outer][inner] (row_bytes apart), no swizzle,
+// boxes of 32 x 32 elements: the output side of tiled bulk stores.
+bool encode_tensor_map_2d_store(CUtensorMap* map, void* base, uint64_t inner, uint64_t outer,
+                                uint64_t row_bytes);
+
 // 3-D TMA tensor map of fp32 [d2][d1][d0] (d0 contiguous), 128-byte swizzle,
 // boxes of 32 x 32 x 1 elements: the output side of tiled bulk stores.
 bool encode_tensor_map_f32_3d(CUtensorMap* map, void* base, uint64_t d0, uint64_t d1, uint64_t d2,
@@ -66,24 +71,31 @@ cudaError_t launch_lse_merge_sharded(const void* partials, int nvt_shard,
 // dz[t][v] = grad[t] * ([v == target[t]] - exp(z[t][v] - lse[t])) as bf16
 // (0 for rows whose target lies outside [0, V)); dz is [T][ldz] row-major with
 // ldz = backward_dz_ld(V) (rows start on 16-byte boundaries, as TMA needs).
+// With tdzt (a 2-D bf16 map of dzt [V][backward_dz_ld(T)], boxes of 32 x 32,
+// no swizzle) the same values are also stored transposed, dzt[v][t].
 cudaError_t launch_lmhead_grad_logits(const CUtensorMap* th, const CUtensorMap* tw,
-                                      const int32_t* targets, const float* lse, const float* grad,
-                                      void* dz, int64_t ldz, int64_t T, int64_t V, int64_t H,
-                                      float inv_temp, int num_sms, cudaStream_t stream);
+                                      const CUtensorMap* tdzt, const int32_t* targets,
+                                      const float* lse, const float* grad, void* dz, int64_t ldz,
+                                      int64_t T, int64_t V, int64_t H, float inv_temp, int num_sms,
+                                      cudaStream_t stream);
 
-// Row stride (elements) of dz: V rounded up to a multiple of 8.
+// Row stride (elements) of dz: V rounded up to a multiple of 8 (of its
+// transposed copy: backward_dz_ld(T)).
 int64_t backward_dz_ld(int64_t V);
+// 2-D map of the transposed dz for launch_lmhead_grad_logits.
+bool encode_dzt_store_map(CUtensorMap* map, void* dzt, int64_t T, int64_t V);
 // Workspace bytes the grad_h product needs for its K-range partial sums (0 if
 // it runs as one range); a function of the shape alone.
 size_t backward_split_bytes(int64_t T, int64_t H, int64_t V);
 
 // grad_h [T][H] = inv_temp * dz . W and grad_W [V][H] (+)= inv_temp * dz^T . h
 // with fp32 accumulation on the tensor cores (either output may be null);
-// dz [T][backward_dz_ld(V)] bf16; split_ws holds backward_split_bytes(T, H, V)
-// bytes (16-byte aligned, as are grad_h and grad_W).
-cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, int64_t T, int64_t H,
-                               int64_t V, float inv_temp, float* grad_h, float* grad_W,
-                               bool accumulate_W, void* split_ws, int num_sms,
+// dz [T][backward_dz_ld(V)] bf16 and, for grad_W, its transpose dzt
+// [V][backward_dz_ld(T)]; split_ws holds backward_split_bytes(T, H, V) bytes
+// (16-byte aligned, as are grad_h and grad_W).
+cudaError_t run_backward_gemms(const void* h, const void* W, const void* dz, const void* dzt,
+                               int64_t T, int64_t H, int64_t V, float inv_temp, float* grad_h,
+                               float* grad_W, bool accumulate_W, void* split_ws, int num_sms,
                                cudaStream_t stream);
 // Reads and clears the backward GEMM kernel's per-device error word (bit 0: a
 // bounded wait ran out; bit 1: a teardown wait ran out).

@@ -85,9 +85,12 @@ struct Pipe {
     // after the barriers: TMEM slot, abort flag, the odd CTA's issue count and
     // its bytes per stage slot (written into the even CTA's words at teardown)
     static constexpr int kWords = 3 + kStages;
+    // backward only: one 32 x 32 bf16 block per epilogue warp, the transposed
+    // copy of dz on its way to a tiled bulk store
+    static constexpr int kTransBytes = 4 * 32 * 32 * 2;
     static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ +
-                                         size_t(kStages) * kStageBytes + kBarriers * 8 +
-                                         kWords * 4 + 16;
+                                         size_t(kStages) * kStageBytes + kTransBytes +
+                                         kBarriers * 8 + kWords * 4 + 16;
     static constexpr int kMmaM = kPair ? 2 * kBM : kBM;
     static constexpr int kEpiArrivals = kPair ? 8 : 4;  // epilogue warps releasing a buffer
     static_assert(kStageBytes % 1024 == 0, "stage tiles 1024-B aligned");
@@ -111,6 +114,7 @@ struct Args {
     const float* grad;     // mode 1: upstream gradient of logp per row
     uint16_t* dz;          // mode 1: [T][ldz] bf16 gradient of logp w.r.t. the logits
     int64_t ldz;           // mode 1: row stride of dz (a multiple of 8 elements)
+    int write_dzt;         // mode 1: also store dz transposed through tmap_x ([V][T])
     int64_t T;
     int64_t h_rows; // rows the h tensor map covers (>= T; padded copies are longer)
     int a_rows;     // rows of each h box (lmhead_a_box_rows(T))
@@ -217,7 +221,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int kMode, bool kFp8, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmap_h,
-                  const __grid_constant__ CUtensorMap tmap_w, const Args p) {
+                  const __grid_constant__ CUtensorMap tmap_w,
+                  const __grid_constant__ CUtensorMap tmap_x, const Args p) {
     static_assert(!kFp8 || kMode == kModePartials, "fp8 operands: forward partials only");
     using P = Pipe<kPair>;
     constexpr int kG = kPair ? 2 : 1;  // tcgen05 CTA group
@@ -232,7 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
     uint8_t* smem = smem_raw + pad;
     const uint32_t tiles_addr = raw_addr + pad;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes);
+    uint16_t* trans = reinterpret_cast<uint16_t*>(smem + size_t(kStages) * kStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes +
+                                                 P::kTransBytes);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBarriers);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // tmem_slot[2]: the odd CTA's issue count; tmem_slot[3 + s]: its bytes in slot s
@@ -606,6 +613,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float g = valid ? __ldg(p.grad + row) : 0.0f;
                 const float lse2 = live ? __ldg(p.lse + row) * kLog2e : 0.0f;
                 uint16_t* dz_row = p.dz + (live ? row : 0) * p.ldz;  // 16-byte aligned rows
+                // transposed copy: this warp's 32 rows x 32 columns of a chunk are
+                // staged as 32 columns x 32 rows and stored in one piece
+                uint16_t* tblk = trans + q * 32 * 32;
+                const int row0 = int(int64_t(m) * kBM + q * 32);  // this warp's first row
+                const bool warp_live = int64_t(row0) < p.T;
                 for (int c = 0; c < nchunks; ++c) {
                     uint32_t r[32];
                     tmem_ld32(t_addr + uint32_t(c * 32), r);
@@ -625,6 +637,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         packed[j / 2] = pack_bf16x2(d0, d1);
                     }
                     const int nvalid = ncols - c * 32;
+                    if (p.write_dzt && warp_live) {
+                        if (lane == 0) bulk_wait_group_read<0>();  // previous block read out
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            tblk[j * 32 + lane] =
+                                uint16_t((packed[j / 2] >> (16 * (j & 1))) & 0xFFFFu);
+                        fence_proxy_async_shared();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmap_x, smem_u32(tblk), row0, cbase);
+                            bulk_commit_group();
+                        }
+                    }
                     if (live && nvalid >= 32) {
                         uint4* dst = reinterpret_cast<uint4*>(dz_row + cbase);
 #pragma unroll
@@ -654,6 +680,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         }
+        if constexpr (kMode == kModeGradLogits) {
+            if (p.write_dzt && lane == 0) bulk_wait_group<0>();  // every store has completed
+            __syncwarp();
+        }
     }
 
     tc_fence_before_sync();
@@ -675,8 +705,8 @@ struct VariantState {
 VariantState g_variant[8][64];  // per kernel variant and device
 
 template <int kMode, bool kFp8, bool kPair>
-cudaError_t launch_variant(const CUtensorMap* th, const CUtensorMap* tw, Args a, int64_t H,
-                           int num_sms, cudaStream_t stream) {
+cudaError_t launch_variant(const CUtensorMap* th, const CUtensorMap* tw, const CUtensorMap* tx,
+                           Args a, int64_t H, int num_sms, cudaStream_t stream) {
     using P = Pipe<kPair>;
     constexpr int kVariant = (kFp8 ? 3 : kMode) + (kPair ? 4 : 0);
     constexpr int kBKE = kFp8 ? 2 * kBK : kBK;
@@ -731,20 +761,22 @@ cudaError_t launch_variant(const CUtensorMap* th, const CUtensorMap* tw, Args a,
     } else {
         cfg.gridDim = dim3(a.num_tiles < num_sms ? a.num_tiles : num_sms, 1, 1);
     }
-    e = cudaLaunchKernelEx(&cfg, kernel, *th, *tw, a);
+    e = cudaLaunchKernelEx(&cfg, kernel, *th, *tw, *tx, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-// Calls with more than one row tile run the CTA-pair variant.
+// Calls with more than one row tile run the CTA-pair variant.  tx: the map of
+// the transposed dz (backward with write_dzt); any valid map otherwise.
 template <int kMode, bool kFp8 = false>
 cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, int64_t H,
-                        int num_sms, cudaStream_t stream) {
+                        int num_sms, cudaStream_t stream, const CUtensorMap* tx = nullptr) {
     if (a.h_rows == 0) a.h_rows = a.T;
     a.a_rows = lmhead_a_box_rows(a.T);
+    if (!tx) tx = tw;
     if (lmhead_use_pair(a.T))
-        return launch_variant<kMode, kFp8, true>(th, tw, a, H, num_sms, stream);
-    return launch_variant<kMode, kFp8, false>(th, tw, a, H, num_sms, stream);
+        return launch_variant<kMode, kFp8, true>(th, tw, tx, a, H, num_sms, stream);
+    return launch_variant<kMode, kFp8, false>(th, tw, tx, a, H, num_sms, stream);
 }
 
 }  // namespace
@@ -809,19 +841,21 @@ cudaError_t launch_lmhead_stall_selftest(const CUtensorMap* th, const CUtensorMa
 }
 
 cudaError_t launch_lmhead_grad_logits(const CUtensorMap* th, const CUtensorMap* tw,
-                                      const int32_t* targets, const float* lse, const float* grad,
-                                      void* dz, int64_t ldz, int64_t T, int64_t V, int64_t H,
-                                      float inv_temp, int num_sms, cudaStream_t stream) {
+                                      const CUtensorMap* tdzt, const int32_t* targets,
+                                      const float* lse, const float* grad, void* dz, int64_t ldz,
+                                      int64_t T, int64_t V, int64_t H, float inv_temp, int num_sms,
+                                      cudaStream_t stream) {
     Args a = {};
     a.targets = targets;
     a.lse = lse;
     a.grad = grad;
     a.dz = static_cast<uint16_t*>(dz);
     a.ldz = ldz;
+    a.write_dzt = tdzt ? 1 : 0;
     a.T = T;
     a.V = int(V);
     a.inv_temp = inv_temp;
-    return launch_mode<kModeGradLogits>(th, tw, a, H, num_sms, stream);
+    return launch_mode<kModeGradLogits>(th, tw, a, H, num_sms, stream, tdzt);
 }
 
 cudaError_t lmhead_take_error(unsigned int* out) {

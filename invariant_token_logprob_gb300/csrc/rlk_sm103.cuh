@@ -176,6 +176,15 @@ __device__ __forceinline__ void tma_load_2d_hint(const void* desc, uint32_t bar,
         : "memory");
 }
 
+// 2-D tiled bulk tensor store shared -> global, tracked as a bulk async-group
+// of the issuing thread.  Elements of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void* desc, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     desc),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 3-D tiled bulk tensor store shared -> global, tracked as a bulk async-group
 // of the issuing thread.  Elements of the box outside the tensor are not
 // written.  (x, y, z) = element coordinates, innermost first.
