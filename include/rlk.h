@@ -119,7 +119,11 @@ size_t rlk_logprob_workspace_size(int64_t T, int64_t H, int64_t V);
  * Workspace: a per-(device, stream) buffer kept by the library, grown with
  * cudaMallocAsync on `stream` when a call needs more, released by
  * rlk_shutdown().  Two calls that share a stream share that buffer in stream
- * order, which is safe; use rlk_logprob_ws to supply your own workspace.
+ * order, which is safe; use rlk_logprob_ws to supply your own workspace.  The
+ * cache is not pruned: every stream that ever called rlk_logprob keeps its
+ * buffer (up to T * ceil(V/256) * 16 bytes * 1.25) until rlk_shutdown, also
+ * after the stream is destroyed.  Engines that create streams per request
+ * should use rlk_logprob_ws.
  */
 rlk_status rlk_logprob(const void *hidden_bf16, const void *weight_bf16,
                        const int32_t *targets_i32, int64_t T, int64_t H, int64_t V,
