@@ -105,6 +105,10 @@ __global__ void __launch_bounds__(kQuantThreads)
                          int H, uint8_t* __restrict__ codes, float* __restrict__ scales,
                          int64_t scale_rows) {
     static_assert(kTpr == 32 || kTpr == kQuantThreads, "a warp or the whole CTA per row");
+    // h quantisation is launched with programmatic overlap: nothing global is
+    // read or written before the previous kernel in the stream has completed
+    // (a no-op for launches without it).
+    grid_dependency_wait();
     grid_launch_dependents();
     const int t = threadIdx.x % kTpr;
     const int64_t r = int64_t(blockIdx.x) * (kQuantThreads / kTpr) + threadIdx.x / kTpr;
@@ -245,6 +249,7 @@ __global__ void __launch_bounds__(kQuantThreads)
     quantize_row_blocks_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
                                int64_t out_rows, int H, uint8_t* __restrict__ codes,
                                float* __restrict__ scales) {
+    grid_dependency_wait();  // launched with programmatic overlap (see quantize_rows_kernel)
     grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t r = int64_t(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
@@ -366,10 +371,21 @@ __global__ void __launch_bounds__(kQuantThreads)
 
 cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_rows, int64_t H,
                                      void* codes, float* scales, cudaStream_t stream) {
-    // one CTA per row: a decode step quantises a handful of rows and waits for it
-    quantize_rows_kernel<false, kQuantThreads><<<unsigned(out_rows), kQuantThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), rows, out_rows, int(H),
-        static_cast<uint8_t*>(codes), scales, out_rows);
+    // one CTA per row: a decode step quantises a handful of rows and waits for
+    // it, so its launch overlaps the end of the previous kernel in the stream
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(unsigned(out_rows), 1, 1);
+    cfg.blockDim = dim3(kQuantThreads, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_rows_kernel<false, kQuantThreads>,
+                                       static_cast<const __nv_bfloat16*>(x), rows, out_rows, int(H),
+                                       static_cast<uint8_t*>(codes), scales, out_rows);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -413,9 +429,19 @@ cudaError_t launch_quantize_fp8_row_blocks(const void* x, int64_t rows, int64_t 
                                            void* codes, float* scales, cudaStream_t stream) {
     constexpr int kRowsPerCta = kQuantThreads / 32;  // one warp per row
     const int64_t ctas = (out_rows + kRowsPerCta - 1) / kRowsPerCta;
-    quantize_row_blocks_kernel<<<unsigned(ctas), kQuantThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), rows, out_rows, int(H), static_cast<uint8_t*>(codes),
-        scales);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(unsigned(ctas), 1, 1);
+    cfg.blockDim = dim3(kQuantThreads, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_row_blocks_kernel,
+                                       static_cast<const __nv_bfloat16*>(x), rows, out_rows, int(H),
+                                       static_cast<uint8_t*>(codes), scales);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
