@@ -1,25 +1,11 @@
-// rlk_merge.cu -- fixed-tree merge of per-(row, vocabulary tile) partials into
-// the row's LSE, argmax and selected-token logprob.
-//
-// The RL-Kernel blog ("大模型强化学习后训练：如何通过 RL-Kernel 彻底消除训推 LogP
-// 偏差", §七 "LogP") merges per-shard local statistics in a fixed
-// vocabulary-tile order; §四 gives the blockwise LSE merge it relies on.  Here
-// one warp owns one row:
-//   lane l folds tiles l, l+32, l+64, ... left to right (lse_combine), then the
-//   32 lane results meet in a 5-step xor butterfly (16, 8, 4, 2, 1).
-// The tree depends only on NVT = ceil(V / 256), never on T, and lse_combine is
-// commutative bit for bit, so all lanes finish with identical bits.
-//   lse = M + log(S),  argmax = A,  logp = zt(tile of target) - lse
-// (logp = 0 for a target outside [0, V); a target >= V is also counted in a
-// per-device word that rlk_check_device_error reports: unlike a negative
-// target it is no "ignore" marker but an out-of-range index).  The entropy
-// variant also folds u = sum exp(z - m)(z - m) per tile and writes
-// entropy = log S - U / S, the softmax entropy -sum p log p over the whole
-// vocabulary.
+// rlk_merge.cu -- the merge kernel: one warp per row folds the row's
+// per-(row, vocabulary tile) partials into its LSE, argmax and selected-token
+// logprob along the fixed tree of merge_row (rlk_merge_row.cuh: the RL-Kernel
+// blog's fixed vocabulary-tile order, §七, over its blockwise LSE merge, §四).
 #include <limits.h>
 
 #include "rlk_internal.h"
-#include "rlk_lse.cuh"
+#include "rlk_merge_row.cuh"
 #include "rlk_sm103.cuh"
 
 namespace rlk {
@@ -35,19 +21,6 @@ __device__ unsigned long long g_target_range_rows;
 
 namespace {
 
-// Record of global tile j for `row`: [T][nvt] unsharded, or [R][T][nvt_shard]
-// when the partials were gathered from vocabulary shards.
-template <bool kSharded>
-__device__ __forceinline__ const float4* record(const float4* partials, int64_t row, int64_t T,
-                                                int nvt, int nvt_shard, int j) {
-    if constexpr (kSharded) {
-        const int r = j / nvt_shard;
-        return partials + (int64_t(r) * T + row) * nvt_shard + (j - r * nvt_shard);
-    } else {
-        return partials + row * nvt + j;
-    }
-}
-
 // kEntropy: also fold the per-tile entropy statistic u (same tree, same winner
 // rule) and write entropy = log S - U / S.  kSharded: records gathered from
 // vocabulary shards (same global tiles, same fold order, same bits).
@@ -60,63 +33,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
                      int nvt_shard = 0) {
     // Launched with programmatic overlap: wait for the producer of the partials
     // before reading anything, then let the next kernel start its launch.
+    // (Triggering before the wait measured slower for decode: the next LM-head
+    // kernel's CTAs then land during this one's producer's tail and their L2
+    // prefetches compete with its last tiles.)
     grid_dependency_wait();
     grid_launch_dependents();
-    const int lane = threadIdx.x & 31;
     const int64_t row = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
     if (row >= T) return;  // whole warp leaves together
-
-    float m = -INFINITY, s = 0.0f, u = 0.0f;
-    int32_t a = INT_MAX;
-    // Lane l folds tiles l, l+32, l+64, ... in ascending order.  The records are
-    // fetched kBatch at a time before folding them (same order, same bits), so a
-    // row with up to 768 tiles costs one memory round trip instead of one per tile.
-    constexpr int kBatch = 24;
-    for (int j0 = lane; j0 < nvt; j0 += 32 * kBatch) {
-        float4 q[kBatch];
-        float uq[kBatch];
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            const int j = j0 + 32 * b;
-            if (j < nvt) {
-                q[b] = __ldg(record<kSharded>(partials, row, T, nvt, nvt_shard, j));
-                if constexpr (kEntropy) uq[b] = __ldg(ent_u + row * nvt + j);
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            if (j0 + 32 * b < nvt) {
-                if constexpr (kEntropy)
-                    u = lse_combine_u(m, s, a, u, q[b].x, q[b].y, __float_as_int(q[b].z), uq[b]);
-                lse_combine(m, s, a, q[b].x, q[b].y, __float_as_int(q[b].z));
-            }
-        }
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-        const float so = __shfl_xor_sync(0xffffffffu, s, off);
-        const int32_t ao = __shfl_xor_sync(0xffffffffu, a, off);
-        if constexpr (kEntropy) {
-            const float uo = __shfl_xor_sync(0xffffffffu, u, off);
-            u = lse_combine_u(m, s, a, u, mo, so, ao, uo);
-        }
-        lse_combine(m, s, a, mo, so, ao);
-    }
-    if (lane == 0) {
-        const float lse = m + logf(s);
-        const int32_t tgt = __ldg(targets + row);
-        float logp = 0.0f;
-        if (tgt >= 0 && tgt < V)
-            logp = __ldg(record<kSharded>(partials, row, T, nvt, nvt_shard, tgt / kVocabTile)).w -
-                   lse;
-        else if (tgt >= V)
-            atomicAdd(&g_target_range_rows, 1ull);
-        out_logp[row] = logp;
-        out_lse[row] = lse;
-        out_argmax[row] = a;
-        if constexpr (kEntropy) out_entropy[row] = logf(s) - u / s;
-    }
+    const MergeOut o = {out_logp, out_lse, out_argmax, out_entropy, &g_target_range_rows};
+    merge_row<kEntropy, kSharded>(partials, ent_u, targets, row, T, V, nvt, nvt_shard, o);
 }
 
 template <bool kEntropy, bool kSharded>

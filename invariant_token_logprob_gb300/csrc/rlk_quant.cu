@@ -107,9 +107,12 @@ __global__ void __launch_bounds__(kQuantThreads)
     static_assert(kTpr == 32 || kTpr == kQuantThreads, "a warp or the whole CTA per row");
     // h quantisation is launched with programmatic overlap: nothing global is
     // read or written before the previous kernel in the stream has completed
-    // (a no-op for launches without it).
-    grid_dependency_wait();
+    // (a no-op for launches without it).  The next kernel (the LM-head kernel)
+    // may start its launch at once: it touches no global memory before its own
+    // dependency wait, which ends only when this grid has completed, so its
+    // launch and set-up overlap the previous kernel and this one.
     grid_launch_dependents();
+    grid_dependency_wait();
     const int t = threadIdx.x % kTpr;
     const int64_t r = int64_t(blockIdx.x) * (kQuantThreads / kTpr) + threadIdx.x / kTpr;
     if (r >= out_rows) return;  // uniform per row group (warp or CTA)
@@ -249,8 +252,8 @@ __global__ void __launch_bounds__(kQuantThreads)
     quantize_row_blocks_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
                                int64_t out_rows, int H, uint8_t* __restrict__ codes,
                                float* __restrict__ scales) {
-    grid_dependency_wait();  // launched with programmatic overlap (see quantize_rows_kernel)
-    grid_launch_dependents();
+    grid_launch_dependents();  // launched with programmatic overlap (see quantize_rows_kernel)
+    grid_dependency_wait();
     const int lane = threadIdx.x & 31;
     const int64_t r = int64_t(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
     if (r >= out_rows) return;  // uniform per warp

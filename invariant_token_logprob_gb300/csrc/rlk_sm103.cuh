@@ -132,6 +132,15 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(desc) : "memory");
 }
 
+// Bring the 2-D box at (x, y) of a tensor into L2 (no shared memory, no
+// completion to wait for).  L2 is where every write to global memory lands,
+// so a prefetched line can never be stale.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* desc, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(desc),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2-D tiled bulk tensor load global -> shared, completion signalled on `bar`
 // as transaction bytes.  (x, y) = (innermost, outer) element coordinates.
 __device__ __forceinline__ void tma_load_2d(const void* desc, uint32_t bar, uint32_t dst, int x,
