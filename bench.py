@@ -328,13 +328,50 @@ def time_decode(rlk, torch, W, Ts, reps, rounds, stream):
     return {T: statistics.median(v) for T, v in times.items()}
 
 
+def graph_time(torch, call, k=20, replays=5):
+    """Seconds per call of `call(stream)` replayed from a CUDA graph of k calls,
+    as a decode loop captured in a graph runs it (no per-launch host work)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        call(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(k):
+                call(side)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(replays):
+        g.replay()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / (replays * k) * 1e-3
+
+
 def decode_points(rlk, torch, W, stream, pk, Ts=(1, 2, 4, 8, 16, 32, 64, 128, 256), reps=50,
-                  rounds=3):
+                  rounds=3, graph_Ts=(1, 16)):
+    """Eager calls back to back (T{T}) and, for graph_Ts, the same call replayed
+    from a CUDA graph (T{T}_graph); explicit workspaces, so nothing allocates
+    during capture."""
     wbytes = V_CFG * H_CFG * 2
     res = {}
     for T, s in time_decode(rlk, torch, W, Ts, reps, rounds, stream).items():
         res[f"T{T}"] = dict(tokens_per_s=T / s, us_per_call=s * 1e6, hbm_gbs=wbytes / s / 1e9,
                             hbm_frac=wbytes / s / 1e9 / pk["hbm_gbs"])
+    for T in graph_Ts:
+        h = torch.randn(T, H_CFG, device=W.device).to(torch.bfloat16)
+        tg = torch.randint(0, V_CFG, (T,), device=W.device, dtype=torch.int32)
+        out = [torch.empty(T, device=W.device, dtype=dt)
+               for dt in (torch.float32, torch.float32, torch.int32)]
+        ws = torch.empty(rlk.workspace_size(T, H_CFG, V_CFG), dtype=torch.uint8, device=W.device)
+        s = graph_time(torch, lambda st: rlk.logprob_ws(h, W, tg, ws, 1.0, out=out, stream=st))
+        res[f"T{T}_graph"] = dict(tokens_per_s=T / s, us_per_call=s * 1e6,
+                                  hbm_gbs=wbytes / s / 1e9, hbm_frac=wbytes / s / 1e9 / pk["hbm_gbs"])
     return res
 
 
@@ -504,9 +541,18 @@ def fp8_points(rlk, torch, h, W, tg, pk, reps=20):
                                 peak_tflops=peak8, frac=fl / t / 1e12 / peak8,
                                 peak_note="fp8 peak = measured bf16 burst x 2 (nominal ratio)")
     for Td in (1, 16):
-        td = timed(h[:Td].contiguous(), tg[:Td].contiguous(), 50)
+        hh, tt = h[:Td].contiguous(), tg[:Td].contiguous()
+        td = timed(hh, tt, 50)
         res[f"decode_T{Td}"] = dict(tokens_per_s=Td / td, us_per_call=td * 1e6,
                                      hbm_gbs=V * H / td / 1e9, hbm_frac=V * H / td / 1e9 / pk["hbm_gbs"])
+        buf = torch.empty(rlk.fp8_workspace_size(Td, H, V), dtype=torch.uint8, device=h.device)
+        out = [torch.empty(Td, device=h.device, dtype=dt)
+               for dt in (torch.float32, torch.float32, torch.int32)]
+        tg_ = graph_time(torch, lambda st: rlk.logprob_fp8(hh, wq, wsc, tt, 1.0, workspace=buf,
+                                                           out=out, stream=st))
+        res[f"decode_T{Td}_graph"] = dict(tokens_per_s=Td / tg_, us_per_call=tg_ * 1e6,
+                                           hbm_gbs=V * H / tg_ / 1e9,
+                                           hbm_frac=V * H / tg_ / 1e9 / pk["hbm_gbs"])
     rlk.check_device_error()
     return res
 
@@ -595,7 +641,7 @@ def run_decode_only(args):
                                   hbm_frac=V_CFG * H_CFG / t / 1e9 / pk["hbm_gbs"])}
     else:
         res = decode_points(rlk, torch, W, stream, pk, Ts=(args.decode_T,), reps=args.steps,
-                            rounds=1)
+                            rounds=1, graph_Ts=())
     rlk.check_device_error()
     print(json.dumps(dict(mode="decode-only", H=H_CFG, V=V_CFG, **res)), flush=True)
     return 0
