@@ -451,6 +451,20 @@ rlk_status rlk_logprob_fp8(const void* hidden_bf16, const uint8_t* weight_e4m3,
     int dev, sms;
     if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the packed weight as rows of 128 bytes: blocks * kVocabTile of them
+    const int64_t packed_rows = num_vocab_tiles(V) * (H / 128) * kVocabTile;
+    if (rlk::lmhead_fp8_quantises_h(T, H)) {
+        // decode-sized: the LM-head kernel quantises h itself
+        CUtensorMap tw;
+        if (!encode_2d(&tw, weight_e4m3, packed_rows, 128, rlk::lmhead_w_box_rows(T), true))
+            return RLK_ERR_CUDA;
+        cudaError_t e = rlk::launch_lmhead_partials_fp8_hq(&tw, targets_i32, hidden_bf16,
+                                                           weight_scales_f32, workspace, T, V, H,
+                                                           inv_temp, sms, s);
+        if (e != cudaSuccess) return from_cuda(e);
+        return from_cuda(rlk::launch_lse_merge(workspace, targets_i32, T, V, out_logp_f32,
+                                               out_lse_f32, out_argmax_i32, s));
+    }
     const int64_t hrows = fp8_h_rows(T);
     char* base = static_cast<char*>(workspace);
     uint8_t* qh = reinterpret_cast<uint8_t*>(base + partial_bytes(T, V));
@@ -458,8 +472,6 @@ rlk_status rlk_logprob_fp8(const void* hidden_bf16, const uint8_t* weight_e4m3,
     cudaError_t e = rlk::launch_quantize_fp8_rows(hidden_bf16, T, hrows, H, qh, sh, s);
     if (e != cudaSuccess) return from_cuda(e);
     CUtensorMap th, tw;
-    // the packed weight as rows of 128 bytes: blocks * kVocabTile of them
-    const int64_t packed_rows = num_vocab_tiles(V) * (H / 128) * kVocabTile;
     if (!encode_2d(&th, qh, hrows, H, rlk::lmhead_a_box_rows(T), true) ||
         !encode_2d(&tw, weight_e4m3, packed_rows, 128, rlk::lmhead_w_box_rows(T), true))
         return RLK_ERR_CUDA;

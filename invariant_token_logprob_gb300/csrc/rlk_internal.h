@@ -112,6 +112,15 @@ cudaError_t launch_lmhead_partials_fp8(const CUtensorMap* th, const CUtensorMap*
                                        int64_t H, float inv_temp, int num_sms,
                                        cudaStream_t stream);
 
+// Decode-sized fp8 calls (T <= 4, H <= 4096): the LM-head kernel quantises the
+// bf16 h [T][H] itself (the quantiser kernel's arithmetic: the same codes and
+// row scales), so no quantiser launch and no h tensor map are needed.
+bool lmhead_fp8_quantises_h(int64_t T, int64_t H);
+cudaError_t launch_lmhead_partials_fp8_hq(const CUtensorMap* tw, const int32_t* targets,
+                                          const void* h, const float* sw, void* partials,
+                                          int64_t T, int64_t V, int64_t H, float inv_temp,
+                                          int num_sms, cudaStream_t stream);
+
 // Per-row e4m3 quantisation of bf16 x [rows][H] into codes [out_rows][H] and
 // scales [out_rows]; rows >= `rows` are zero codes with scale 1.  H % 16 == 0.
 cudaError_t launch_quantize_fp8_rows(const void* x, int64_t rows, int64_t out_rows, int64_t H,

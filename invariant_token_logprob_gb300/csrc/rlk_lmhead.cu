@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 #include <limits.h>
 
+#include "rlk_fp8_quant.cuh"
 #include "rlk_internal.h"
 #include "rlk_lse.cuh"
 #include "rlk_sm103.cuh"
@@ -62,6 +63,11 @@ constexpr int kAccBufs = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kThreads = 192;
+// kHq: calls of at most kHqMaxRows rows with H <= kHqMaxH quantise h in the
+// kernel; the codes sit in a block of kHqRows rows (the 16-row box layout)
+constexpr int kHqRows = kMinTmaRows;
+constexpr int kHqMaxRows = 4;
+constexpr int kHqMaxH = 4096;
 
 // Per-CTA pipeline shape.  Single CTA: the CTA stages a 128-row h block and the
 // whole 256-row W block of each k-block (48 KiB), one k-block per stage, four
@@ -71,23 +77,32 @@ constexpr int kThreads = 192;
 // halve the barrier rounds and commits per MMA, which measured ~8% fewer cycles
 // than six one-k-block stages in the compute-bound regime; in the weight-
 // streaming (decode) regime the single CTA's smaller stages measured better.
-template <bool kPair>
+//
+// kHq (single CTA, e4m3, a handful of rows): the CTA quantises the call's h
+// rows itself into a resident shared-memory block of kHqRows rows x H codes
+// (laid out as the 16-row TMA boxes would land), and the stages carry W only.
+template <bool kPair, bool kHq = false>
 struct Pipe {
+    static_assert(!(kPair && kHq), "in-kernel h quantisation: single CTA only");
     static constexpr int kBRows = kPair ? kBN / 2 : kBN;  // W rows one CTA stages
     static constexpr int kBBytes = kBRows * kBK * 2;
-    static constexpr int kKbBytes = kABytes + kBBytes;    // one k-block: h block + W block
+    static constexpr int kAStageBytes = kHq ? 0 : kABytes;  // h block per staged k-block
+    static constexpr int kKbBytes = kAStageBytes + kBBytes;  // one k-block: h block + W block
     static constexpr int kKbPerStage = kPair ? 2 : 1;     // k-blocks per stage (one barrier)
     static constexpr int kStageBytes = kKbPerStage * kKbBytes;
     static constexpr int kStages = kPair ? 3 : 4;
     // full / empty per stage, tfull / tempty per accumulator, drain, and for the
-    // CTA pair's teardown hand-shake odd_done (even CTA) and drained (odd CTA)
-    static constexpr int kBarriers = 2 * kStages + 2 * kAccBufs + 3;
+    // CTA pair's teardown hand-shake odd_done (even CTA) and drained (odd CTA);
+    // kHq: h ready
+    static constexpr int kBarriers = 2 * kStages + 2 * kAccBufs + 3 + (kHq ? 1 : 0);
     // after the barriers: TMEM slot, abort flag, the odd CTA's issue count and
-    // its bytes per stage slot (written into the even CTA's words at teardown)
-    static constexpr int kWords = 3 + kStages;
+    // its bytes per stage slot (written into the even CTA's words at teardown);
+    // kHq: then the row scales and the epilogue warps' partial row maxima
+    static constexpr int kWords = 3 + kStages + (kHq ? kHqRows + 4 * kHqMaxRows : 0);
     // backward only: one 32 x 32 bf16 block per epilogue warp, the transposed
     // copy of dz on its way to a tiled bulk store
     static constexpr int kTransBytes = 4 * 32 * 32 * 2;
+    // kHq adds kHqRows * H bytes of h codes in front of the stages
     static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ +
                                          size_t(kStages) * kStageBytes + kTransBytes +
                                          kBarriers * 8 + kWords * 4 + 16;
@@ -138,6 +153,7 @@ struct Args {
                          // 2, the MMA issuer consumes no stage
     const float* sh;     // fp8 operands: per-row scale of h [rows]
     const float* sw;     // fp8 operands: per-row scale of W [V] (this launch's rows)
+    const __nv_bfloat16* h;  // kHq: the bf16 h rows [T][H], quantised by the kernel
 };
 
 // Raster over (row unit, vocabulary tile): bands of `band` row units; inside a
@@ -205,6 +221,94 @@ constexpr int kModePartials = 0;   // forward: vocabulary-tile partial records
 constexpr int kModeGradLogits = 1; // backward: dz = g (onehot - exp(z - lse)) as bf16
 constexpr int kModeEntropy = 2;    // forward records plus the per-tile entropy statistic
 
+// kHq: the call's T (<= kHqMaxRows) h rows of H (<= kHqMaxH, a multiple of 128)
+// bf16 -> e4m3 codes in the resident block `hq` and the row scales in
+// hq_scale[0, T), by the 128 epilogue threads together (t = 0..127).  Thread t
+// converts the 16-element groups t and t + 128 of every row; all rows are
+// loaded at once.  A row's max meets in shuffles, then across the four warps
+// in shared memory (a max: exact in any order); the scale, the division and
+// the conversion are the quantiser kernel's, so the codes and scales are the
+// same bits.  Group g of row r is stored where the 16-row SW128 TMA box of its
+// k-block g / 8 would put it: row r at 128 * r (8-row groups 1024 bytes
+// apart), its 16-byte chunk g % 8 at (g % 8) ^ (r % 8).  Ends with the
+// epilogue warps' barrier, after which codes and scales are complete.
+__device__ __forceinline__ void quantise_h_rows(const __nv_bfloat16* __restrict__ h, int T, int H,
+                                                int t, uint8_t* hq, float* hq_scale) {
+    constexpr int kGroups = kHqMaxH / 16 / 128;  // 16-element groups per thread and row
+    float* wmax = hq_scale + kHqRows;           // [4 warps][kHqMaxRows]
+    const int ngroups = H / 16;
+    uint4 v[kHqMaxRows][kGroups][2];
+#pragma unroll
+    for (int r = 0; r < kHqMaxRows; ++r)
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i) {
+            const int g = t + 128 * i;
+            if (r < T && g < ngroups) {
+                const uint4* src = reinterpret_cast<const uint4*>(h + int64_t(r) * H + g * 16);
+                v[r][i][0] = __ldg(src);
+                v[r][i][1] = __ldg(src + 1);
+            } else {
+                v[r][i][0] = v[r][i][1] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    const int lane = t & 31;
+#pragma unroll
+    for (int r = 0; r < kHqMaxRows; ++r) {
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[r][i][half]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __bfloat1622float2(b[j]);
+                    amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+            }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (lane == 0) wmax[(t >> 5) * kHqMaxRows + r] = amax;
+    }
+    named_barrier_sync(1, 128);
+#pragma unroll
+    for (int r = 0; r < kHqMaxRows; ++r) {
+        if (r >= T) break;
+        const float amax = fmaxf(fmaxf(wmax[r], wmax[kHqMaxRows + r]),
+                                 fmaxf(wmax[2 * kHqMaxRows + r], wmax[3 * kHqMaxRows + r]));
+        const float sc = e4m3_scale(amax);
+        const bool fast = sc >= kE4m3FastScaleMin;
+        const float rs = fast ? __frcp_rn(sc) : 0.0f;
+        uint8_t* row_base = hq + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i) {
+            const int g = t + 128 * i;
+            if (g >= ngroups) continue;
+            uint32_t out[4];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[r][i][half]);
+                const float2 f0 = __bfloat1622float2(b[0]), f1 = __bfloat1622float2(b[1]);
+                const float2 f2 = __bfloat1622float2(b[2]), f3 = __bfloat1622float2(b[3]);
+                if (fast) {
+                    out[2 * half] = e4m3x4<true>(f0.x, f0.y, f1.x, f1.y, sc, rs);
+                    out[2 * half + 1] = e4m3x4<true>(f2.x, f2.y, f3.x, f3.y, sc, rs);
+                } else {
+                    out[2 * half] = e4m3x4<false>(f0.x, f0.y, f1.x, f1.y, sc, rs);
+                    out[2 * half + 1] = e4m3x4<false>(f2.x, f2.y, f3.x, f3.y, sc, rs);
+                }
+            }
+            const int c = g & 7;
+            *reinterpret_cast<uint4*>(row_base + (g >> 3) * (kHqRows * 128) + ((c ^ (r & 7)) << 4)) =
+                make_uint4(out[0], out[1], out[2], out[3]);
+        }
+        if (t == 0) hq_scale[r] = sc;
+    }
+    fence_proxy_async_shared();  // the codes are read by the tensor core
+    named_barrier_sync(1, 128);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
@@ -225,13 +329,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // K steps in the same order and the same epilogue; only the MMA instruction's
 // M (which rows it covers, never how one row is summed) and the copy routes
 // differ.
-template <int kMode, bool kFp8, bool kPair>
+//
+// kHq (e4m3, single CTA, T <= kHqMaxRows, H <= kHqMaxH): h arrives as bf16
+// (p.h) and the epilogue warps quantise it before the first MMA with the
+// quantiser kernel's arithmetic (same codes, same row scales), so a decode call
+// needs no quantiser launch; tmap_h is then unused.
+template <int kMode, bool kFp8, bool kPair, bool kHq = false>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmap_h,
                   const __grid_constant__ CUtensorMap tmap_w,
                   const __grid_constant__ CUtensorMap tmap_x, const Args p) {
     static_assert(!kFp8 || kMode == kModePartials, "fp8 operands: forward partials only");
-    using P = Pipe<kPair>;
+    static_assert(!kHq || (kFp8 && !kPair), "in-kernel h quantisation: e4m3, single CTA");
+    using P = Pipe<kPair, kHq>;
     constexpr int kG = kPair ? 2 : 1;  // tcgen05 CTA group
     constexpr int kStages = P::kStages;
     constexpr int kStageBytes = P::kStageBytes;
@@ -242,8 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
-    uint8_t* smem = smem_raw + pad;
-    const uint32_t tiles_addr = raw_addr + pad;
+    // kHq: the h codes come first (a multiple of 1024 bytes); an MMA reading a
+    // 128-row operand from a late k-block runs into the stages, never past them
+    const uint32_t hq_bytes = kHq ? uint32_t(kHqRows) * uint32_t(p.num_kb) * 128u : 0u;
+    const uint32_t hq_addr = raw_addr + pad;
+    uint8_t* smem = smem_raw + pad + hq_bytes;
+    const uint32_t tiles_addr = raw_addr + pad + hq_bytes;
     uint16_t* trans = reinterpret_cast<uint16_t*>(smem + size_t(kStages) * kStageBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes +
                                                  P::kTransBytes);
@@ -251,6 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // tmem_slot[2]: the odd CTA's issue count; tmem_slot[3 + s]: its bytes in slot s
     volatile uint32_t* odd_words = tmem_slot + 2;
+    // kHq: row scales [kHqRows], then the epilogue warps' row maxima [4][kHqMaxRows]
+    float* hq_scale = reinterpret_cast<float*>(tmem_slot + 3 + kStages);
 
     auto full_bar = [&](int s) { return smem_u32(bars + s); };
     auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
@@ -259,11 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 2 * kAccBufs);
     const uint32_t odd_done_bar = drain_bar + 8;  // even CTA: the odd CTA stopped issuing
     const uint32_t drained_bar = drain_bar + 16;  // odd CTA: every copy of the pair landed
-    // k-block j of stage s: h block, then W block
+    const uint32_t hq_bar = drain_bar + 24;       // kHq: h codes and scales written
+    // k-block j of stage s: h block (unless kHq), then W block
     auto a_tile = [&](int s, int j) {
         return tiles_addr + uint32_t(s) * kStageBytes + uint32_t(j) * P::kKbBytes;
     };
-    auto b_tile = [&](int s, int j) { return a_tile(s, j) + kABytes; };
+    auto b_tile = [&](int s, int j) { return a_tile(s, j) + P::kAStageBytes; };
+    // kHq: k-block kb of the resident h codes (kHqRows rows of 128 bytes)
+    auto hq_tile = [&](int kb) { return hq_addr + uint32_t(kb) * uint32_t(kHqRows * 128); };
     constexpr int kKbs = P::kKbPerStage;
 
     const int warp = threadIdx.x >> 5;
@@ -281,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(drain_bar, 1);
         mbar_init(odd_done_bar, 1);
         mbar_init(drained_bar, 1);
+        if constexpr (kHq) mbar_init(hq_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -347,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tile) is not copied; the MMA then reads stale shared memory for
                 // rows / columns that the epilogues never report.
                 // per k-block: single CTA, its h box and W block; CTA pair, each CTA's
-                uint32_t bytes_r[2] = {uint32_t(p.a_rows) * 128u + P::kBBytes, 0u};
+                uint32_t bytes_r[2] = {(kHq ? 0u : uint32_t(p.a_rows) * 128u) + P::kBBytes, 0u};
                 bool load_a = true, load_b = true;
                 if constexpr (kPair) {
 #pragma unroll
@@ -395,8 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(full_bar(stage), uint32_t(nkb) * bytes_r[0]);
                         for (int j = 0; j < nkb; ++j) {
                             const int kb = kb0 + j;
-                            tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage, j), kb * kBKE,
-                                        m * kBM);
+                            if constexpr (!kHq)
+                                tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage, j), kb * kBKE,
+                                            m * kBM);
                             if constexpr (kFp8)  // tile-packed weight: one contiguous 32 KB block
                                 tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage, j), 0,
                                             (n * p.num_kb + kb) * kBN);
@@ -466,7 +587,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             // Self-test 2: no stage is consumed, so the producers fill the ring,
             // then wait for a free stage until their limit runs out.
-            const int ntiles = p.stall_selftest == 2 ? 0 : p.num_tiles;
+            int ntiles = p.stall_selftest == 2 ? 0 : p.num_tiles;
+            if constexpr (kHq) {
+                // the h codes, written by the epilogue warps, before the first MMA
+                if (!wait_bounded(hq_bar, 0, abort_flag)) ntiles = 0;
+                tc_fence_after_sync();
+            }
             for (int tile = slot; ok && tile < ntiles; tile += nslots) {
                 if (!wait_bounded<kPair>(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after_sync();
@@ -480,7 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int nkb = min(kKbs, p.num_kb - kb0);
                     for (int j = 0; j < nkb; ++j) {
                         const int kb = kb0 + j;
-                        const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage, j));
+                        const uint64_t a_desc =
+                            sw128_kmajor_desc(kHq ? hq_tile(kb) : a_tile(stage, j));
                         const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage, j));
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
@@ -528,6 +655,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16);
         const float inv_temp = p.inv_temp;
         uint32_t acc = 0, acc_phase = 0;
+        if constexpr (kHq) {
+            quantise_h_rows(p.h, int(p.T), p.num_kb * 128, threadIdx.x - 64, smem_raw + pad,
+                            hq_scale);
+            if (warp == 2 && lane == 0) mbar_arrive(hq_bar);  // after quantise_h_rows' barrier
+        }
         for (int tile = slot; tile < p.num_tiles; tile += nslots) {
             int mu, n;
             tile_coords(p, tile, mu, n);
@@ -544,7 +676,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int col = n * kBN + 32 * i + lane;
                     col_scale[i] = col < p.V ? __ldg(p.sw + col) : 0.0f;
                 }
-                row_scale = row < p.T ? __ldg(p.sh + row) : 0.0f;
+                if constexpr (kHq)
+                    row_scale = row < p.T ? hq_scale[row] : 0.0f;
+                else
+                    row_scale = row < p.T ? __ldg(p.sh + row) : 0.0f;
             }
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag) ? 1 : 0;
@@ -728,15 +863,16 @@ struct VariantState {
     int configured = 0;    // dynamic shared memory attribute set
     int max_clusters = 0;  // CTA pairs that fit at once (CTA-pair variants)
 };
-VariantState g_variant[8][64];  // per kernel variant and device
+VariantState g_variant[9][64];  // per kernel variant and device
+constexpr size_t kMaxSmemBytes = 227 * 1024;
 
-template <int kMode, bool kFp8, bool kPair>
+template <int kMode, bool kFp8, bool kPair, bool kHq = false>
 cudaError_t launch_variant(const CUtensorMap* th, const CUtensorMap* tw, const CUtensorMap* tx,
                            Args a, int64_t H, int num_sms, cudaStream_t stream) {
-    using P = Pipe<kPair>;
-    constexpr int kVariant = (kFp8 ? 3 : kMode) + (kPair ? 4 : 0);
+    using P = Pipe<kPair, kHq>;
+    constexpr int kVariant = kHq ? 8 : (kFp8 ? 3 : kMode) + (kPair ? 4 : 0);
     constexpr int kBKE = kFp8 ? 2 * kBK : kBK;
-    auto kernel = lmhead_kernel<kMode, kFp8, kPair>;
+    auto kernel = lmhead_kernel<kMode, kFp8, kPair, kHq>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -752,14 +888,14 @@ cudaError_t launch_variant(const CUtensorMap* th, const CUtensorMap* tw, const C
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = P::kSmemBytes;
+    cfg.dynamicSmemBytes = P::kSmemBytes + (kHq ? size_t(kHqRows) * size_t(H) : 0);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = kPair ? 2 : 1;
 
     if (!vs.configured) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(P::kSmemBytes));
+                                 int(kHq ? kMaxSmemBytes : P::kSmemBytes));
         if (e != cudaSuccess) return e;
         if constexpr (kPair) {
             // how many CTA pairs the GPU holds at once (pairs need two SMs of
@@ -800,6 +936,11 @@ cudaError_t launch_mode(const CUtensorMap* th, const CUtensorMap* tw, Args a, in
     if (a.h_rows == 0) a.h_rows = a.T;
     a.a_rows = lmhead_a_box_rows(a.T);
     if (!tx) tx = tw;
+    if constexpr (kFp8 && kMode == kModePartials) {
+        // bf16 h given: the kernel quantises it (no h tensor map; tw stands in)
+        if (a.h != nullptr) return launch_variant<kMode, true, false, true>(tw, tw, tx, a, H,
+                                                                            num_sms, stream);
+    }
     if (lmhead_use_pair(a.T))
         return launch_variant<kMode, kFp8, true>(th, tw, tx, a, H, num_sms, stream);
     return launch_variant<kMode, kFp8, false>(th, tw, tx, a, H, num_sms, stream);
@@ -833,6 +974,28 @@ cudaError_t launch_lmhead_entropy(const CUtensorMap* th, const CUtensorMap* tw,
     a.V = int(V);
     a.inv_temp = inv_temp;
     return launch_mode<kModeEntropy>(th, tw, a, H, num_sms, stream);
+}
+
+bool lmhead_fp8_quantises_h(int64_t T, int64_t H) {
+    static_assert(Pipe<false, true>::kSmemBytes + size_t(kHqRows) * kHqMaxH <= kMaxSmemBytes,
+                  "h codes and weight stages fit in shared memory");
+    return T >= 1 && T <= kHqMaxRows && H <= kHqMaxH && H % 128 == 0;
+}
+
+cudaError_t launch_lmhead_partials_fp8_hq(const CUtensorMap* tw, const int32_t* targets,
+                                          const void* h, const float* sw, void* partials,
+                                          int64_t T, int64_t V, int64_t H, float inv_temp,
+                                          int num_sms, cudaStream_t stream) {
+    if (!lmhead_fp8_quantises_h(T, H)) return cudaErrorInvalidValue;
+    Args a = {};
+    a.targets = targets;
+    a.partials = static_cast<float4*>(partials);
+    a.sw = sw;
+    a.h = static_cast<const __nv_bfloat16*>(h);
+    a.T = T;
+    a.V = int(V);
+    a.inv_temp = inv_temp;
+    return launch_mode<kModePartials, true>(nullptr, tw, a, H, num_sms, stream);
 }
 
 cudaError_t launch_lmhead_partials_fp8(const CUtensorMap* th, const CUtensorMap* tw,

@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include "rlk_fp8_quant.cuh"
 #include "rlk_internal.h"
 #include "rlk_sm103.cuh"
 
@@ -36,38 +37,6 @@ __device__ __forceinline__ int64_t code_offset(int64_t r, int k, int H) {
     } else {
         return r * int64_t(H) + k;
     }
-}
-
-// x / sc rounded to nearest, from rs = the correctly rounded 1 / sc: the
-// product's residual is exact under fma, and one correction step gives the
-// correctly rounded quotient (Markstein, "Computation of elementary functions on
-// the IBM RISC System/6000 processor", 1990).  The quotient has the sign of x
-// whatever it rounds to, so the sign is copied from x: that keeps -0 for x = -0
-// (the correction step alone gives +0 there) with one bit operation instead of
-// a compare and a select (measured 4% faster for the weight).  Callers use it
-// only while rs is finite and normal; the GPU tests check it against the IEEE
-// division for every bf16 x and every scale amax/448 a bf16 amax can give.
-__device__ __forceinline__ float div_by_scale(float x, float sc, float rs) {
-    const float q = __fmul_rn(x, rs);
-    const float e = __fmaf_rn(-q, sc, x);
-    return copysignf(__fmaf_rn(e, rs, q), x);
-}
-
-template <bool kFast>
-__device__ __forceinline__ float quotient(float x, float sc, float rs) {
-    if constexpr (kFast)
-        return div_by_scale(x, sc, rs);
-    else
-        return __fdiv_rn(x, sc);
-}
-
-template <bool kFast>
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d, float sc, float rs) {
-    const uint32_t c0 = __nv_cvt_float_to_fp8(quotient<kFast>(a, sc, rs), __NV_SATFINITE, __NV_E4M3);
-    const uint32_t c1 = __nv_cvt_float_to_fp8(quotient<kFast>(b, sc, rs), __NV_SATFINITE, __NV_E4M3);
-    const uint32_t c2 = __nv_cvt_float_to_fp8(quotient<kFast>(c, sc, rs), __NV_SATFINITE, __NV_E4M3);
-    const uint32_t c3 = __nv_cvt_float_to_fp8(quotient<kFast>(d, sc, rs), __NV_SATFINITE, __NV_E4M3);
-    return c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
 }
 
 // Pass 2 of a row: divide, convert, store 16 codes per thread and step.
@@ -149,8 +118,8 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
         for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
     }
-    const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    if (sc >= 0x1p-64f)
+    const float sc = e4m3_scale(amax);
+    if (sc >= kE4m3FastScaleMin)
         convert_row<kTiled, true, kTpr>(xr, r, H, t, sc, __frcp_rn(sc), codes);
     else
         convert_row<kTiled, false, kTpr>(xr, r, H, t, sc, 0.0f, codes);
@@ -231,8 +200,8 @@ __global__ void __launch_bounds__(kStagedWarps * 32, 1)
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1)
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        if (sc >= 0x1p-64f)
+        const float sc = e4m3_scale(amax);
+        if (sc >= kE4m3FastScaleMin)
             convert_row<true, true, 32>(xr, r, H, lane, sc, __frcp_rn(sc), codes);
         else
             convert_row<true, false, 32>(xr, r, H, lane, sc, 0.0f, codes);
@@ -282,8 +251,8 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
         for (int off = 4; off >= 1; off >>= 1)  // the 8 lanes of this 128-element block
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        const bool fast = sc >= 0x1p-64f;
+        const float sc = e4m3_scale(amax);
+        const bool fast = sc >= kE4m3FastScaleMin;
         const float rs = fast ? __frcp_rn(sc) : 0.0f;
         uint32_t out[4];
 #pragma unroll
@@ -345,8 +314,8 @@ __global__ void __launch_bounds__(kQuantThreads)
     amax = warp_max[0];
 #pragma unroll
     for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
-    const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    const bool fast = sc >= 0x1p-64f;
+    const float sc = e4m3_scale(amax);
+    const bool fast = sc >= kE4m3FastScaleMin;
     const float rs = fast ? __frcp_rn(sc) : 0.0f;
     uint32_t out[16];
 #pragma unroll

@@ -132,6 +132,12 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(desc) : "memory");
 }
 
+// Barrier `id` (1..15; 0 is __syncthreads) over `threads` threads of the CTA
+// (a multiple of 32, whole warps).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Bring the 2-D box at (x, y) of a tensor into L2 (no shared memory, no
 // completion to wait for).  L2 is where every write to global memory lands,
 // so a prefetched line can never be stale.

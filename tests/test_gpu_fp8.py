@@ -134,6 +134,34 @@ def test_fp8_pair_and_single_cta_calls_agree_bitwise():
         assert_bitwise(full, got, f"fp8 T=300 chunk={c}")
 
 
+@pytest.mark.parametrize("H", [128, 384, 4096, 5120])
+def test_fp8_decode_calls_quantise_h_in_the_kernel(olib, H):
+    """Calls of at most 4 rows with H <= 4096 quantise h inside the LM-head
+    kernel (H = 5120 takes the quantiser kernel).  Same codes and scales as the
+    quantiser, so every row's bits must equal those of a 40-row call (quantiser
+    kernel, single CTA), including an all-zero row and a row whose scale takes
+    the IEEE-division path, and the rows must match the oracle on the
+    quantiser's codes."""
+    import invariant_token_logprob_gb300 as rlk
+    T, V = 40, 700
+    d = to_dev(lm_head_inputs(T, H, V, seed=H))
+    d["h"][5] = 0.0                                  # all-zero row: scale 1, codes 0
+    d["h"][6] *= 1e-30                               # tiny row: the IEEE-division path
+    d["h"][7, ::3] = -d["h"][7, ::3]
+    wq, ws = rlk.quantize_fp8_weight(d["W"])
+    full = _np(rlk.logprob_fp8(d["h"], wq, ws, d["targets"]))
+    for c in (1, 2, 3, 4, 16):
+        parts = [_np(rlk.logprob_fp8(d["h"][i:i + c].contiguous(), wq, ws,
+                                     d["targets"][i:i + c].contiguous())) for i in range(0, T, c)]
+        got = tuple(np.concatenate([p[k] for p in parts]) for k in range(3))
+        assert_bitwise(full, got, f"fp8 H={H} chunk={c}")
+    rlk.check_device_error()
+    qh, sh = oracle.quantize_fp8_rows(d["h"].cpu(), lib=olib)
+    qw, sw = oracle.quantize_fp8_rows(d["W"].cpu(), lib=olib)
+    ref = oracle.logprob_fp8(qh, sh, qw, sw, d["targets"].cpu(), 1.0, lib=olib)
+    assert_parity(full, ref, what=f"fp8 H={H}")
+
+
 @pytest.mark.slow
 def test_fp8_full_size_parity_and_invariance(olib):
     import invariant_token_logprob_gb300 as rlk
