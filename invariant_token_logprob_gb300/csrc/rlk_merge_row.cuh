@@ -5,8 +5,11 @@
 // 偏差", §七 "LogP") merges per-shard local statistics in a fixed
 // vocabulary-tile order; §四 gives the blockwise LSE merge it relies on.  The
 // tree:
-//   lane l folds tiles l, l+32, l+64, ... left to right (lse_combine), then the
-//   32 lane results meet in a 5-step xor butterfly (16, 8, 4, 2, 1).
+//   lane l holds tiles l, l+32, ..., l+32*23 in 24 slots (an absent tile is the
+//   combine's identity) and folds them in a fixed pairwise tree; rows of more
+//   than 768 tiles repeat this per group of 24 slots, the groups folded left to
+//   right; then the 32 lane results meet in a 5-step xor butterfly (16, 8, 4,
+//   2, 1).
 // It depends only on NVT = ceil(V / 256), never on T, and lse_combine is
 // commutative bit for bit, so all lanes finish with identical bits.
 //   lse = M + log(S),  argmax = A,  logp = zt(tile of target) - lse
@@ -69,27 +72,41 @@ __device__ __forceinline__ void merge_row(const float4* __restrict__ partials,
     // row with up to 768 tiles costs one memory round trip instead of one per tile.
     constexpr int kBatch = 24;
     for (int j0 = lane; j0 < nvt; j0 += 32 * kBatch) {
-        float4 q[kBatch];
-        float uq[kBatch];
+        float qm[kBatch], qs[kBatch], uq[kBatch];
+        int32_t qa[kBatch];
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
             const int j = j0 + 32 * b;
+            qm[b] = -INFINITY;  // the identity of the combine for an absent tile
+            qs[b] = 0.0f;
+            qa[b] = INT_MAX;
+            uq[b] = 0.0f;
             if (j < nvt) {
-                q[b] = __ldg(merge_record<kSharded>(partials, row, T, nvt, nvt_shard, j));
+                const float4 r = __ldg(merge_record<kSharded>(partials, row, T, nvt, nvt_shard, j));
+                qm[b] = r.x;
+                qs[b] = r.y;
+                qa[b] = __float_as_int(r.z);
                 if constexpr (kEntropy) uq[b] = __ldg(ent_u + row * nvt + j);
             }
         }
         if (j0 == lane && tgt_in)  // first pass (lane 0 always has one: nvt >= 1)
             zt = __ldg(
                 &merge_record<kSharded>(partials, row, T, nvt, nvt_shard, tgt / kVocabTile)->w);
+        // Pairwise tree over the kBatch slots: level w combines slots b and
+        // b + w into b (b a multiple of 2w).  Five levels instead of a chain
+        // of up to 24 dependent combines; the shape is fixed at compile time.
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            if (j0 + 32 * b < nvt) {
+        for (int w = 1; w < kBatch; w *= 2) {
+#pragma unroll
+            for (int b = 0; b + w < kBatch; b += 2 * w) {
                 if constexpr (kEntropy)
-                    u = lse_combine_u(m, s, a, u, q[b].x, q[b].y, __float_as_int(q[b].z), uq[b]);
-                lse_combine(m, s, a, q[b].x, q[b].y, __float_as_int(q[b].z));
+                    uq[b] = lse_combine_u(qm[b], qs[b], qa[b], uq[b], qm[b + w], qs[b + w],
+                                          qa[b + w], uq[b + w]);
+                lse_combine(qm[b], qs[b], qa[b], qm[b + w], qs[b + w], qa[b + w]);
             }
         }
+        if constexpr (kEntropy) u = lse_combine_u(m, s, a, u, qm[0], qs[0], qa[0], uq[0]);
+        lse_combine(m, s, a, qm[0], qs[0], qa[0]);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
