@@ -156,9 +156,11 @@ rlk_status rlk_logprob_partials(const void *hidden_bf16, const void *weight_bf16
 /*
  * Phase 2 alone: merge each row's NVT = ceil(V / rlk_vocab_tile()) partials
  * in a fixed tree (the fixed vocabulary-tile-order merge of the RL-Kernel
- * blog, §七 "LogP").  Per row: lane l of one warp folds tiles l, l+32, l+64, ...
- * in ascending order, then five butterfly steps (xor 16, 8, 4, 2, 1) combine
- * lanes.  The combine of (m1,s1,a1) and (m2,s2,a2) keeps the larger m (the
+ * blog, §七 "LogP").  Per row: lane l of one warp holds tiles l, l+32, ...,
+ * l+32*23 in 24 slots (an absent tile is the combine's identity) and folds them
+ * in a fixed pairwise tree (slots b and b+w into b, w = 1, 2, 4, 8, 16); rows
+ * of more than 768 tiles repeat this per group of 24 slots and fold the groups
+ * in order; then five butterfly steps (xor 16, 8, 4, 2, 1) combine lanes.  The combine of (m1,s1,a1) and (m2,s2,a2) keeps the larger m (the
  * lower a on equal m) as M and forms S = s_win + s_lose * exp(m_lose - M); it
  * is commutative bit for bit, so every lane ends with the same bits.
  * lse = M + log S, argmax = A, logp = zt(target's tile) - lse (0.0f for an

@@ -67,9 +67,9 @@ __device__ __forceinline__ void merge_row(const float4* __restrict__ partials,
     const int32_t tgt = __ldg(targets + row);
     const bool tgt_in = tgt >= 0 && tgt < V;
     float zt = 0.0f;
-    // Lane l folds tiles l, l+32, l+64, ... in ascending order.  The records are
-    // fetched kBatch at a time before folding them (same order, same bits), so a
-    // row with up to 768 tiles costs one memory round trip instead of one per tile.
+    // Lane l holds tiles l, l+32, l+64, ... in kBatch slots.  All of a group's
+    // records are fetched before any is folded, so a row with up to 768 tiles
+    // costs one memory round trip instead of one per tile.
     constexpr int kBatch = 24;
     for (int j0 = lane; j0 < nvt; j0 += 32 * kBatch) {
         float qm[kBatch], qs[kBatch], uq[kBatch];
