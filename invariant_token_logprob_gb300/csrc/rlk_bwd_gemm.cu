@@ -398,6 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16);
         const float alpha = p.alpha;
+        // the output is written once and not read back here: evict it first
+        const uint64_t store_policy = l2_policy_evict_first();
         // This warp's staging block: its 32 rows x 32 columns of one chunk,
         // written in the 128-byte-swizzled layout the tensor store reads
         // (16-byte piece i of row r at piece i ^ (r % 8)), which also keeps
@@ -439,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0 && row0 < p.M) {
-                        tma_store_3d(&tmap_d, out_block, col0 + c * 32, row0, s);
+                        tma_store_3d_hint(&tmap_d, out_block, col0 + c * 32, row0, s,
+                                          store_policy);
                         bulk_commit_group();
                     }
                 } else if (live) {

@@ -210,6 +210,25 @@ __device__ __forceinline__ void tma_store_3d(const void* desc, uint32_t src, int
         "r"(src), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
+// An L2 cache policy under which the lines an access brings in or writes are
+// the first to be evicted: for output the kernel does not read again, so it
+// does not push out operands that other CTAs are about to reuse.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    return policy;
+}
+
+// tma_store_3d with an L2 cache policy (l2_policy_evict_first, ...).
+__device__ __forceinline__ void tma_store_3d_hint(const void* desc, uint32_t src, int x, int y,
+                                                  int z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint"
+        " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(desc),
+        "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
