@@ -41,6 +41,7 @@ def test_tiny_full_parity_and_forced_ties(olib):
 @pytest.mark.parametrize("T,H,V,seed", [
     (1, 64, 1, 1), (3, 8, 257, 2), (130, 72, 1000, 3), (257, 136, 2049, 4),
     (5, 4096, 3000, 5), (129, 512, 512, 6), (300, 64, 33, 7), (2, 1024, 151936, 8),
+    (6, 64, 250000, 9),  # 977 tiles a row: the merge folds two groups of 24 slots per lane
 ])
 def test_ragged_shapes(T, H, V, seed, olib):
     d = to_dev(lm_head_inputs(T, H, V, seed=seed))
@@ -140,11 +141,13 @@ def test_partials_match_oracle_block_stats(olib):
     assert_block_records(P, bs, d["h"], d["W"], rlk.vocab_tile(), what="partials")
 
 
-def test_merge_alone_matches_oracle_fp64_merge(olib):
-    """Phase 2 alone on synthetic partials (including -inf blocks and equal maxima)."""
+@pytest.mark.parametrize("V", [151936, 250000, 1000003])
+def test_merge_alone_matches_oracle_fp64_merge(olib, V):
+    """Phase 2 alone on synthetic partials (including -inf blocks and equal
+    maxima).  V = 250000 and 1000003 give rows of 977 and 3907 tiles: the merge
+    folds more than one group of 24 slots per lane."""
     import invariant_token_logprob_gb300 as rlk
     g = np.random.default_rng(4)
-    V = 151936
     nvt = (V + 255) // 256
     T = 333
     m = g.normal(0, 3, (T, nvt)).astype(np.float32)
