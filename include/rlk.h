@@ -233,7 +233,10 @@ rlk_status rlk_lse_merge_sharded(const rlk_partial *partials, int64_t num_shards
  *   rlk_fp8_weight_bytes(V, H) bytes, scales V floats.  H % 128 == 0.
  *   Asynchronous; run once per weight update.
  * rlk_logprob_fp8: quantise h per row into the workspace, then the fp8 LM-head
- *   kernel and the fixed-tree merge.  weight_e4m3 / weight_scales_f32 as
+ *   kernel and the fixed-tree merge.  Calls of at most 4 rows with H <= 4096
+ *   (decode) skip the separate quantisation: the LM-head kernel converts the
+ *   rows itself with the same arithmetic, so the codes, scales and results are
+ *   the same bits either way (the workspace size does not change).  weight_e4m3 / weight_scales_f32 as
  *   produced by rlk_quantize_fp8_weight; workspace >=
  *   rlk_logprob_fp8_workspace_size(T, H, V), 16-byte aligned.  Other arguments
  *   and outputs as rlk_logprob_ws; H % 128 == 0 (else RLK_ERR_ALIGNMENT).
