@@ -34,6 +34,11 @@
 //     block; a 3-stage ring of 64 KB holding two k-blocks per stage (one
 //     barrier round and one commit per 8 MMAs); grid sized by the occupancy
 //     of clusters.
+// Weight-streaming (single-CTA) launches also bring the first k-blocks of
+// their first W tile into L2 before their dependency wait, and e4m3 calls of
+// at most 4 rows quantise h in the kernel (template parameter kHq): the
+// epilogue warps write the codes into a resident shared-memory block before
+// the first MMA, and the ring then carries W only.
 // The accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue
 // of tile i overlaps the MMAs of tile i+1.  Every wait is bounded in time.
 #include <cuda_bf16.h>
