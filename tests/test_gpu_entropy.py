@@ -39,7 +39,8 @@ def _ent(d, it=1.0):
 
 
 @pytest.mark.parametrize("case", ["tiny", (1, 64, 1, 1), (7, 72, 1000, 2), (130, 256, 2049, 3),
-                                  (300, 128, 33, 4)])
+                                  (300, 128, 33, 4),
+                                  (6, 64, 250000, 5)])  # 977 tiles a row: two slot groups per lane
 def test_entropy_matches_oracle_and_forward_bits(case, olib):
     import invariant_token_logprob_gb300 as rlk
     if case == "tiny":

@@ -44,7 +44,8 @@ def _sharded(rlk, d, V, R, it=1.0):
     return buf, nvt_s
 
 
-@pytest.mark.parametrize("T,H,V", [(70, 256, 3000), (5, 512, 151936), (300, 128, 257)])
+@pytest.mark.parametrize("T,H,V", [(70, 256, 3000), (5, 512, 151936), (300, 128, 257),
+                                   (4, 64, 250000)])  # rows of 977 tiles
 def test_sharded_merge_equals_unsharded_for_every_shard_count(T, H, V):
     import invariant_token_logprob_gb300 as rlk
     d = to_dev(lm_head_inputs(T, H, V, seed=T))
