@@ -181,16 +181,6 @@ __device__ __forceinline__ void tma_load_2d_pair(const void* desc, uint32_t bar_
         : "memory");
 }
 
-// Same with an L2 cache-eviction policy (from createpolicy).
-__device__ __forceinline__ void tma_load_2d_hint(const void* desc, uint32_t bar, uint32_t dst,
-                                                 int x, int y, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(desc), "r"(bar), "r"(x), "r"(y), "l"(policy)
-        : "memory");
-}
-
 // 2-D tiled bulk tensor store shared -> global, tracked as a bulk async-group
 // of the issuing thread.  Elements of the box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const void* desc, uint32_t src, int x, int y) {
@@ -246,18 +236,6 @@ __device__ __forceinline__ void bulk_wait_group() {
 // async-proxy (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 
 // ---------------------------------------------------------------- tcgen05
