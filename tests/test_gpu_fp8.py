@@ -180,3 +180,8 @@ def test_fp8_full_size_parity_and_invariance(olib):
     assert_bitwise(full, tuple(np.concatenate([p[k] for p in seq]) for k in range(3)), "fp8 8x512")
     one = _np(rlk.logprob_fp8(d["h"][7:8].contiguous(), wq, ws, d["targets"][7:8].contiguous()))
     assert_bitwise(tuple(x[7:8] for x in full), one, "fp8 T=1 vs T=4096")
+    # 4 rows: the largest call whose h the LM-head kernel quantises itself
+    four = _np(rlk.logprob_fp8(d["h"][100:104].contiguous(), wq, ws,
+                               d["targets"][100:104].contiguous()))
+    assert_bitwise(tuple(x[100:104] for x in full), four, "fp8 T=4 vs T=4096")
+    rlk.check_device_error()
