@@ -324,6 +324,8 @@ rlk_status rlk_logprob_entropy(const void *hidden_bf16, const void *weight_bf16,
  *   grad_h    = inv_temp * dz . W         [T][H] fp32 (overwritten)
  *   grad_W    = inv_temp * dz^T . h       [V][H] fp32 (overwritten, or added to
  *                                          when accumulate_grad_weight != 0)
+ * T == 0: an overwritten grad_W is set to zero (the empty sum; a stream-ordered
+ * memset, the only work done), an accumulated one is left as it is.
  * The logits are recomputed on the forward's fixed tiles (same main loop, so
  * the same fp32 logits), p uses the forward's lse, dz is rounded once to bf16
  * and the two products run as bf16 x bf16 -> fp32 tensor-core GEMMs of this

@@ -626,7 +626,16 @@ rlk_status rlk_logprob_backward(const void* hidden_bf16, const void* weight_bf16
                                 size_t workspace_bytes, rlk_stream_t stream) {
     rlk_status st = check_shape(T, H, V, inv_temp);
     if (st != RLK_OK) return st;
-    if (T == 0) return RLK_OK;
+    if (T == 0) {
+        // No rows: grad_h is empty and grad_W an empty sum, so an overwritten
+        // grad_W becomes zero and an accumulated one stays as it is.
+        if (!grad_weight_f32 || accumulate_grad_weight) return RLK_OK;
+        if (!aligned16(grad_weight_f32)) return RLK_ERR_ALIGNMENT;
+        int dev, sms;
+        if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
+        return from_cuda(cudaMemsetAsync(grad_weight_f32, 0, size_t(V) * size_t(H) * sizeof(float),
+                                         reinterpret_cast<cudaStream_t>(stream)));
+    }
     if ((st = check_operands(hidden_bf16, weight_bf16, targets_i32, H)) != RLK_OK) return st;
     if (!lse_f32 || !grad_logp_f32) return RLK_ERR_INVALID_ARG;
     if (!aligned4(lse_f32) || !aligned4(grad_logp_f32) || !aligned16(grad_hidden_f32) ||

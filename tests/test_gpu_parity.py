@@ -288,3 +288,37 @@ def test_caller_workspace_matches_cached_workspace(T):
     with pytest.raises(rlk.RlkError) as ei:
         rlk.logprob_ws(d["h"], d["W"], d["targets"], ws[:need - 1])
     assert ei.value.status == 5
+
+
+def test_zero_rows_everywhere():
+    """T = 0 is a valid call for every entry point: empty outputs, nothing
+    launched, no error.  The backward's grad_W is then an empty sum: when it is
+    overwritten it becomes zero, when it is accumulated into it stays as it was."""
+    import ctypes
+    import invariant_token_logprob_gb300 as rlk
+    H, V = 256, 1000
+    d = to_dev(lm_head_inputs(4, H, V, seed=3))
+    h0, tg0, W = d["h"][:0].contiguous(), d["targets"][:0].contiguous(), d["W"]
+    outs = [rlk.logprob(h0, W, tg0),
+            rlk.logprob_fp8(h0, *rlk.quantize_fp8_weight(W), tg0),
+            rlk.logprob_fp8_block(h0, *rlk.quantize_fp8_weight_blocks(W), tg0, V),
+            rlk.logprob_entropy(h0, W, tg0)]
+    parts = rlk.logprob_partials(h0, W, tg0)
+    outs.append(rlk.lse_merge(parts, tg0, V))
+    assert parts.shape[0] == 0
+    for out in outs:
+        assert all(x.numel() == 0 for x in out)
+    L = rlk.lib()
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    gW = torch.full((V, H), float("nan"), device="cuda")
+    assert L.rlk_logprob_backward(None, None, None, None, None, 0, H, V, ctypes.c_float(1.0), None,
+                                  ctypes.c_void_p(gW.data_ptr()), 0, None, 0, st) == 0
+    torch.cuda.synchronize()
+    assert torch.all(gW == 0)
+    base = torch.randn(V, H, device="cuda")
+    gW = base.clone()
+    assert L.rlk_logprob_backward(None, None, None, None, None, 0, H, V, ctypes.c_float(1.0), None,
+                                  ctypes.c_void_p(gW.data_ptr()), 1, None, 0, st) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(gW, base)
+    rlk.check_device_error()
