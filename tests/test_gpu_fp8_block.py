@@ -79,7 +79,10 @@ def _quantised(rlk, d):
 @pytest.mark.parametrize("T,H,V,it", [(64, 256, 1000, 1.0),
                                       (300, 512, 3000, float(np.float32(1 / 0.7))),
                                       (5, 128, 257, 2.0),
-                                      (130, 384, 700, 1.0)])
+                                      (130, 384, 700, 1.0),
+                                      # CTA pair: the last vocabulary tile's odd half lies
+                                      # past V (not copied), one k block
+                                      (200, 128, 2100, 1.0)])
 def test_block_fp8_logprob_matches_oracle(olib, T, H, V, it):
     import invariant_token_logprob_gb300 as rlk
     d = to_dev(lm_head_inputs(T, H, V, seed=T + H, hidden="normal", w_std=0.05))
