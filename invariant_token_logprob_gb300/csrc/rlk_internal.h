@@ -30,7 +30,7 @@ int lmhead_a_box_rows(int64_t T);
 // 2-D TMA tensor map, 128-byte swizzle, zero fill outside the matrix: `outer`
 // rows of `inner` elements (bf16, or bytes when `bytes`), row_bytes apart
 // (a multiple of 16), boxes of box_inner x box_outer elements (box_inner *
-// element size <= 128).  False if the driver refuses it.
+// element size <= 128).  False if the CUDA driver refuses it.
 bool encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                           uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool bytes);
 
