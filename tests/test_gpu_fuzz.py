@@ -15,6 +15,8 @@ For each shape:
   entropy within the entropy tests' tolerance of the oracle's;
 - the vocabulary cut into R shards of whole tiles (R random, every shard
   non-empty), merged, gives the forward's bits.
+Ten smaller shapes (H a multiple of 128) take the backward and both FP8
+formats through the same kind of check.
 """
 import numpy as np
 import pytest
@@ -109,3 +111,71 @@ def test_random_shape(olib, T, H, V, it, seed):
     got = _np(rlk.lse_merge_sharded(buf, dd["targets"], V))
     rlk.check_device_error()
     assert_bitwise(full, got, f"{what}: {R} shards")
+
+
+def _small_shapes(n=10, seed=20261204):
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        T = int(g.choice([1, 4, 5, 128, 129, 256]) if i % 2 else g.integers(1, 301))
+        H = int(128 * g.integers(1, 7))
+        V = int(g.choice([1, 255, 257, 4097]) if i % 3 == 0 else g.integers(1, 6001))
+        it = float(np.float32(g.uniform(0.5, 2.0)))
+        out.append((T, H, V, it, 2000 + i))
+    return out
+
+
+@pytest.mark.parametrize("T,H,V,it,seed", _small_shapes())
+def test_random_shape_backward_and_fp8(olib, T, H, V, it, seed):
+    """Ten smaller random shapes (H a multiple of 128, as the fp8 formats need):
+    the backward's dz, grad_h and grad_W within the backward tests' bf16 error
+    model of the oracle; per-row and block FP8 logprobs against their oracle
+    modes on the codes and scales the GPU quantisers wrote (which must equal
+    the oracle's bit for bit)."""
+    import invariant_token_logprob_gb300 as rlk
+    d = lm_head_inputs(T, H, V, seed=seed, hidden="normal", w_std=0.05)
+    dd = to_dev(d)
+    what = f"T={T} H={H} V={V} inv_temp={it}"
+
+    # backward, with the same bounds as the backward tests
+    grad = torch.randn(T, generator=torch.Generator().manual_seed(seed)).float()
+    _, lse, _ = rlk.logprob(dd["h"], dd["W"], dd["targets"], it)
+    gh, gW, ws = rlk.logprob_backward(dd["h"], dd["W"], dd["targets"], lse, grad.cuda(), it)
+    rlk.check_device_error()
+    dz = rlk.backward_dz(ws, T, V).float().cpu().numpy().astype(np.float64)
+    ref = oracle.logprob_backward(d["h"], d["W"], d["targets"], grad.double().numpy(), it,
+                                  lib=olib)
+    hf = d["h"].float().numpy().astype(np.float64)
+    Wf = d["W"].float().numpy().astype(np.float64)
+    g = grad.double().numpy()
+    assert np.all(np.abs(dz - ref["dz"]) <= 2.0 ** -8 * np.abs(ref["dz"]) + 2e-5 * np.abs(g)[:, None]), \
+        f"{what}: dz"
+    bh = it * 2.0 ** -7 * (np.abs(ref["dz"]) @ np.abs(Wf)) + 1e-6
+    assert np.all(np.abs(gh.cpu().numpy() - ref["dh"]) <= bh), f"{what}: grad_h"
+    bw = it * 2.0 ** -7 * (np.abs(ref["dz"]).T @ np.abs(hf)) + 1e-6
+    assert np.all(np.abs(gW.cpu().numpy() - ref["dW"]) <= bw), f"{what}: grad_W"
+
+    # per-row FP8
+    wq, wsc = rlk.quantize_fp8_weight(dd["W"])
+    got = _np(rlk.logprob_fp8(dd["h"], wq, wsc, dd["targets"], it))
+    rlk.check_device_error()
+    qh, sh = oracle.quantize_fp8_rows(d["h"], lib=olib)
+    qw, sw = oracle.quantize_fp8_rows(d["W"], lib=olib)
+    assert np.array_equal(qw, rlk.unpack_fp8_weight(wq, V, H).cpu().numpy()), f"{what}: W codes"
+    assert np.array_equal(sw.view(np.uint32), wsc.cpu().numpy().view(np.uint32)), f"{what}: W scales"
+    assert_parity(got, oracle.logprob_fp8(qh, sh, qw, sw, d["targets"], it, lib=olib),
+                  what=f"fp8 {what}")
+
+    # block FP8
+    bq, bs = rlk.quantize_fp8_weight_blocks(dd["W"])
+    got = _np(rlk.logprob_fp8_block(dd["h"], bq, bs, dd["targets"], V, it))
+    rlk.check_device_error()
+    hc, hs = rlk.quantize_fp8_row_blocks(dd["h"])
+    rhc, rhs = oracle.quantize_fp8_blocks(d["h"], 1, lib=olib)
+    rwc, rws = oracle.quantize_fp8_blocks(d["W"], 128, lib=olib)
+    assert np.array_equal(hc.cpu().numpy()[:T], rhc) and \
+        np.array_equal(hs.cpu().numpy().view(np.uint32), rhs.view(np.uint32)), f"{what}: h blocks"
+    assert np.array_equal(rlk.unpack_fp8_weight(bq, V, H).cpu().numpy(), rwc) and \
+        np.array_equal(bs.cpu().numpy().view(np.uint32), rws.view(np.uint32)), f"{what}: W blocks"
+    assert_parity(got, oracle.logprob_fp8_block(rhc, rhs, rwc, rws, d["targets"], it, lib=olib),
+                  what=f"block fp8 {what}")
