@@ -66,6 +66,40 @@ def test_block_quantisers_are_bit_exact(olib):
     rlk.check_device_error()
 
 
+def test_block_weight_quantiser_division_is_ieee_on_its_whole_input_domain():
+    """Exhaustive, like the per-row quantiser's test: for every positive finite
+    bf16 amax, one 128-row band of W holds every finite bf16 value with
+    |x| <= amax (the others 0) spread over four 128 x 128 blocks, so the blocks
+    see about 2.1e9 (x, block scale) pairs in all.  The reference takes each
+    block's own max, its scale max / 448 by IEEE division (1 for a zero block)
+    and the codes as torch's float8 e4m3 cast of the IEEE quotient x / scale,
+    all on the same device; scales and codes must match bit for bit, signed
+    zeros included."""
+    import invariant_token_logprob_gb300 as rlk
+    pat = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    base = torch.where(torch.isfinite(pat.float()), pat, torch.zeros_like(pat)).cuda()
+    mags = pat[1:0x7F80].float().cuda()  # every positive finite bf16 value, ascending
+    absb = base.float().abs()
+    A = 512
+    for c0 in range(0, mags.numel(), A):
+        amax = mags[c0:c0 + A]
+        n = amax.numel()
+        vals = torch.where(absb[None, :] <= amax[:, None], base[None, :],
+                           torch.zeros_like(base)[None, :])
+        # band a: block kb holds values kb * 16384 + (row * 128 + col)
+        W = vals.view(n, 4, 128, 128).permute(0, 2, 1, 3).reshape(n * 128, 512).contiguous()
+        packed, scales = rlk.quantize_fp8_weight_blocks(W)
+        codes = rlk.unpack_fp8_weight(packed, n * 128, 512)
+        bmax = W.float().abs().view(n, 128, 4, 128).amax(dim=(1, 3))  # [band, k block]
+        ref_s = torch.where(bmax > 0, bmax / torch.full_like(bmax, 448.0), torch.ones_like(bmax))
+        assert torch.equal(scales.view(torch.int32), ref_s.view(torch.int32)), c0
+        sfull = ref_s[:, None, :, None].expand(n, 128, 4, 128).reshape(n * 128, 512)
+        ref = (W.float() / sfull).to(torch.float8_e4m3fn).view(torch.uint8)
+        bad = (codes != ref).nonzero()
+        assert bad.numel() == 0, (c0, bad[:5].tolist())
+    rlk.check_device_error()
+
+
 def _quantised(rlk, d):
     """GPU block codes/scales of h and W (the ones the kernel reads), on the host."""
     hc, hs = rlk.quantize_fp8_row_blocks(d["h"])
