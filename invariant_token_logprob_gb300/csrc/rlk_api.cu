@@ -750,13 +750,12 @@ rlk_status rlk_take_device_errors(rlk_stream_t stream, uint32_t* wait_error_bits
     if (st != RLK_OK) return st;
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return RLK_ERR_CUDA;
-    unsigned int word = 0, word_bwd = 0, word_fp8b = 0, word_quant = 0;
+    unsigned int word = 0, word_bwd = 0, word_fp8b = 0;
     unsigned long long rows = 0;
     if (rlk::lmhead_take_error(&word) != cudaSuccess) return RLK_ERR_CUDA;
     if (rlk::bwd_gemm_take_error(&word_bwd) != cudaSuccess) return RLK_ERR_CUDA;
     if (rlk::lmhead_fp8b_take_error(&word_fp8b) != cudaSuccess) return RLK_ERR_CUDA;
-    if (rlk::quant_take_error(&word_quant) != cudaSuccess) return RLK_ERR_CUDA;
-    word |= word_bwd | word_fp8b | word_quant;
+    word |= word_bwd | word_fp8b;
     if (rlk::take_target_range_rows(&rows) != cudaSuccess) return RLK_ERR_CUDA;
     if (wait_error_bits) *wait_error_bits = word;
     if (target_range_rows) *target_range_rows = rows;

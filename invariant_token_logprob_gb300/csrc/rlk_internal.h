@@ -152,8 +152,6 @@ cudaError_t launch_lmhead_partials_fp8_block(const CUtensorMap* th, const CUtens
                                              int64_t V, int64_t H, float inv_temp, int num_sms,
                                              cudaStream_t stream);
 cudaError_t lmhead_fp8b_take_error(unsigned int* out);
-// The fp8 weight quantiser's error word (bit 0: a row's copy never landed).
-cudaError_t quant_take_error(unsigned int* out);
 
 // Bounded-wait self-test of the forward kernel (single CTA for T <= 128, CTA
 // pair above): mode 1, its producer issues no copies, so the MMA warp's wait

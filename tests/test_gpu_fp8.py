@@ -73,6 +73,36 @@ def test_quantiser_division_is_ieee_on_its_whole_input_domain():
     rlk.check_device_error()
 
 
+def test_weight_quantiser_division_is_ieee_on_its_whole_input_domain():
+    """Exhaustive for the weight quantiser (rows in registers, H = 4096): for
+    every positive finite bf16 amax, 16 rows of W hold every finite bf16 value
+    with |x| <= amax (the others 0), so the rows see about 2.1e9 (x, row
+    scale) pairs in all.  The reference takes each row's own max, its scale
+    max / 448 by IEEE division (1 for a zero row) and the codes as torch's
+    float8 e4m3 cast of the IEEE quotient x / scale, all on the same device;
+    scales and unpacked codes must match bit for bit, signed zeros included."""
+    import invariant_token_logprob_gb300 as rlk
+    pat = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    base = torch.where(torch.isfinite(pat.float()), pat, torch.zeros_like(pat)).cuda()
+    mags = pat[1:0x7F80].float().cuda()  # every positive finite bf16 value, ascending
+    absb = base.float().abs()
+    A, H = 128, 4096
+    for c0 in range(0, mags.numel(), A):
+        amax = mags[c0:c0 + A]
+        n = amax.numel()
+        W = torch.where(absb[None, :] <= amax[:, None], base[None, :],
+                        torch.zeros_like(base)[None, :]).reshape(n * 16, H).contiguous()
+        packed, scales = rlk.quantize_fp8_weight(W)
+        codes = rlk.unpack_fp8_weight(packed, n * 16, H)
+        rmax = W.float().abs().amax(dim=1)
+        ref_s = torch.where(rmax > 0, rmax / torch.full_like(rmax, 448.0), torch.ones_like(rmax))
+        assert torch.equal(scales.view(torch.int32), ref_s.view(torch.int32)), c0
+        ref = (W.float() / ref_s[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        bad = (codes != ref).nonzero()
+        assert bad.numel() == 0, (c0, bad[:5].tolist())
+    rlk.check_device_error()
+
+
 def test_packed_weight_codes_are_bit_exact_and_padded_with_zeros(olib):
     """The tile-packed fp8 weight holds the oracle's row codes (after unpacking)
     and zero codes in the padding rows of the last vocabulary tile."""
