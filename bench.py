@@ -847,7 +847,7 @@ def run_ours(args):
                     if pk["source"] == "measured" else "fallback 1.9 PFLOP/s",
                     traffic=(tr["bytes_per_launch"] if tr else None),
                     algorithmic_flops_per_launch=flops,
-                    kernel="lmhead_kernel<0, false, true> (bf16 forward partials, CTA pair)", launch_avg_us=gemm_avg * 1e6,
+                    kernel="lmhead_kernel<0, false, true, false> (bf16 forward partials, CTA pair)", launch_avg_us=gemm_avg * 1e6,
                     step_share=gemm_avg * args.steps / (elapsed if world == 1 else elapsed))
     cpu = None
     if not args.no_cpu_baseline and world == 1:
