@@ -103,6 +103,26 @@ def test_weight_quantiser_division_is_ieee_on_its_whole_input_domain():
     rlk.check_device_error()
 
 
+@pytest.mark.parametrize("H", [384, 5120])  # rows in registers / the two-pass kernel (H > 4096)
+def test_weight_quantiser_both_kernels_bit_exact(olib, H):
+    """The weight quantiser keeps a row in one warp's registers up to H = 4096
+    and takes the two-pass kernel above; both must give the oracle's codes and
+    scales, with ragged last tiles (V = 777) and rows of very different
+    magnitude."""
+    import invariant_token_logprob_gb300 as rlk
+    V = 777
+    g = torch.Generator().manual_seed(H)
+    W = (torch.randn(V, H, generator=g) * torch.logspace(-6, 2, V)[:, None]).to(torch.bfloat16)
+    W[5] = 0.0
+    packed, scales = rlk.quantize_fp8_weight(W.cuda())
+    torch.cuda.synchronize()
+    rc, rs = oracle.quantize_fp8_rows(W, lib=olib)
+    assert np.array_equal(rlk.unpack_fp8_weight(packed, V, H).cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    assert torch.all(rlk.unpack_fp8_weight(packed, 1024, H)[V:] == 0)
+    rlk.check_device_error()
+
+
 def test_packed_weight_codes_are_bit_exact_and_padded_with_zeros(olib):
     """The tile-packed fp8 weight holds the oracle's row codes (after unpacking)
     and zero codes in the padding rows of the last vocabulary tile."""
