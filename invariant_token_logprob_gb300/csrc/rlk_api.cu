@@ -547,6 +547,18 @@ rlk_status rlk_logprob_fp8_block(const void* hidden_bf16, const uint8_t* weight_
     int dev, sms;
     if ((st = current_device(&dev, &sms)) != RLK_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t packed_rows_b = num_vocab_tiles(V) * (H / 128) * kVocabTile;
+    if (rlk::lmhead_fp8b_quantises_h(T, H)) {
+        // a few rows: the kernel quantises h itself (same codes and scales)
+        CUtensorMap twq;
+        if (!encode_2d(&twq, weight_e4m3, packed_rows_b, 128, kVocabTile, true))
+            return RLK_ERR_CUDA;
+        cudaError_t eq = rlk::launch_lmhead_partials_fp8_block_hq(
+            &twq, hidden_bf16, targets_i32, weight_scales_f32, workspace, T, V, H, inv_temp, sms, s);
+        if (eq != cudaSuccess) return from_cuda(eq);
+        return from_cuda(rlk::launch_lse_merge(workspace, targets_i32, T, V, out_logp_f32,
+                                               out_lse_f32, out_argmax_i32, s));
+    }
     const int64_t hrows = fp8b_h_rows(T);
     char* base = static_cast<char*>(workspace);
     uint8_t* qh = reinterpret_cast<uint8_t*>(base + partial_bytes(T, V));

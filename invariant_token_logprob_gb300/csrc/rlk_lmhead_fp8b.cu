@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <limits.h>
 
+#include "rlk_fp8_quant.cuh"
 #include "rlk_internal.h"
 #include "rlk_lse.cuh"
 #include "rlk_sm103.cuh"
@@ -46,17 +47,34 @@ constexpr int kBN = kVocabTile;         // 256 vocabulary columns per tile
 constexpr int kHalfN = kBN / 2;         // columns per epilogue thread
 constexpr int kKbBytesW = kBN * 128;    // 32 KB: one packed W block (256 rows x 128 codes)
 constexpr int kAMaxBytes = kBM * 128;   // 16 KB: the largest h box (128 rows x 128 codes)
-constexpr int kStageBytes = kAMaxBytes + kKbBytesW;  // 48 KB
 constexpr int kStages = 4;
+// kHq (calls of at most kHqMaxRows rows, H <= kHqMaxH): the epilogue warps
+// quantise h into a resident block of kHqRows rows in front of the stages,
+// with its block scales; the ring then carries W only.
+constexpr int kHqRows = kMinTmaRows;  // 16: the rows of the resident block
+constexpr int kHqMaxRows = 4;
+constexpr int kHqMaxH = 4096;
+constexpr int kHqCodeBytes = kHqRows * kHqMaxH;              // 64 KB
+constexpr int kHqScaleBytes = kHqMaxRows * (kHqMaxH / 128) * 4;  // 512 B
+constexpr int kHqBytes = kHqCodeBytes + 1024;                  // codes + scales, 1 KB aligned
+static_assert(kHqScaleBytes <= 1024, "h block scales fit their slot");
+template <bool kHq>
+constexpr int stage_bytes() { return (kHq ? 0 : kAMaxBytes) + kKbBytesW; }
 constexpr int kPartBufs = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-// full / empty per stage, pfull / pempty per TMEM buffer, drain
-constexpr int kBarriers = 2 * kStages + 2 * kPartBufs + 1;
-constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kBarriers * 8 + 16 +
-                              2 * kBM * sizeof(float4);  // + the half-record exchange
-static_assert(kStageBytes % 1024 == 0, "stage tiles 1024-B aligned");
+// full / empty per stage, pfull / pempty per TMEM buffer, drain, h written (kHq)
+constexpr int kBarriers = 2 * kStages + 2 * kPartBufs + 2;
+template <bool kHq>
+constexpr size_t smem_bytes() {
+    return 1024 + (kHq ? size_t(kHqBytes) : 0) + size_t(kStages) * stage_bytes<kHq>() +
+           kBarriers * 8 + 16 + 2 * kBM * sizeof(float4);  // + the half-record exchange
+}
+constexpr size_t kSmemBytes = smem_bytes<false>();
+static_assert(stage_bytes<true>() % 1024 == 0 && stage_bytes<false>() % 1024 == 0,
+              "stage tiles 1024-B aligned");
+static_assert(smem_bytes<true>() <= 227 * 1024, "shared memory per CTA (in-kernel h)");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 static_assert(kPartBufs * kBN <= int(kTmemCols), "TMEM budget");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -69,6 +87,7 @@ struct Args {
     float4* partials;   // [T][num_n]
     const float* sh;    // [T][num_kb] activation block scales
     const float* sw;    // [ceil(V/128)][num_kb] weight block scales
+    const __nv_bfloat16* h;  // kHq: the bf16 h rows [T][H], quantised by the kernel
     int64_t T;
     int a_rows;         // rows of each h box
     int V;
@@ -118,18 +137,92 @@ __device__ __forceinline__ void pair_warps_sync(int q) {
     asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
 }
 
+// kHq: two warps per row (at most kHqMaxRows rows), each taking half of the
+// row's 128-element blocks, lane l 16 consecutive elements per step of four
+// blocks; every lane runs every step (the lanes of a block past the half
+// compute on zeros and store nothing), so the shuffles see the whole warp.
+// The block max meets over the block's 8 lanes; then the scale and codes of
+// the block quantiser kernel (same arithmetic, same bits), written at the
+// row's place in the resident 128-byte-swizzled block (16 codes = one 16-byte
+// chunk) and the scale at [row][block].
+__device__ __forceinline__ void quantise_h_blocks(const __nv_bfloat16* __restrict__ h, int T,
+                                                  int H, int w, int lane, uint8_t* hq,
+                                                  float* hq_scale) {
+    const int r = w >> 1;
+    if (r >= T) return;  // whole warps
+    const int nkb = H / 128;
+    const int kb_mid = (nkb + 1) / 2;
+    const int k_begin = (w & 1) ? kb_mid * 128 : 0;
+    const int k_end = (w & 1) ? nkb * 128 : kb_mid * 128;
+    for (int k0 = k_begin; k0 < k_end; k0 += 32 * 16) {
+        const int k = k0 + lane * 16;
+        const bool act = k < k_end;
+        uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+        if (act) {
+            const __nv_bfloat16* xr = h + int64_t(r) * H + k;
+            v0 = __ldg(reinterpret_cast<const uint4*>(xr));
+            v1 = __ldg(reinterpret_cast<const uint4*>(xr + 8));
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(hh ? &v1 : &v0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(p2[i]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+#pragma unroll
+        for (int off = 4; off >= 1; off >>= 1)  // the 8 lanes of this 128-element block
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (!act) continue;
+        const float sc = e4m3_scale(amax);
+        const bool fast = sc >= kE4m3FastScaleMin;
+        const float rs = fast ? __frcp_rn(sc) : 0.0f;
+        uint32_t out[4];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(hh ? &v1 : &v0);
+            const float2 a = __bfloat1622float2(p2[0]), b = __bfloat1622float2(p2[1]);
+            const float2 c = __bfloat1622float2(p2[2]), d = __bfloat1622float2(p2[3]);
+            if (fast) {
+                out[2 * hh] = e4m3x4<true>(a.x, a.y, b.x, b.y, sc, rs);
+                out[2 * hh + 1] = e4m3x4<true>(c.x, c.y, d.x, d.y, sc, rs);
+            } else {
+                out[2 * hh] = e4m3x4<false>(a.x, a.y, b.x, b.y, sc, rs);
+                out[2 * hh + 1] = e4m3x4<false>(c.x, c.y, d.x, d.y, sc, rs);
+            }
+        }
+        const int kb = k >> 7;
+        const int chunk = (k & 127) >> 4;
+        *reinterpret_cast<uint4*>(hq + kb * (kHqRows * 128) + (r >> 3) * 1024 + (r & 7) * 128 +
+                                  ((chunk ^ (r & 7)) << 4)) =
+            make_uint4(out[0], out[1], out[2], out[3]);
+        if ((lane & 7) == 0) hq_scale[r * nkb + kb] = sc;
+    }
+}
+
 // 10 warps put three warps on two of the SM's four sub-partitions (16384
 // registers each), which caps a thread at 168 registers: the epilogue threads
 // keep 128 running sums and load TMEM 16 columns at a time.
+template <bool kHq>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_fp8b_kernel(const __grid_constant__ CUtensorMap tmap_h,
                        const __grid_constant__ CUtensorMap tmap_w, const Args p) {
     constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, kBN);
+    constexpr int kStageBytes = stage_bytes<kHq>();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
-    uint8_t* smem = smem_raw + pad;
-    const uint32_t tiles_addr = raw_addr + pad;
+    // kHq: the resident h codes [k block][16 rows][128 B] and their block
+    // scales [row][k block] come first; an MMA reading 128 rows of h from a
+    // late k block runs into the stages, never past them.
+    uint8_t* hq = smem_raw + pad;
+    float* hq_scale = reinterpret_cast<float*>(hq + kHqCodeBytes);
+    const uint32_t hq_addr = raw_addr + pad;
+    uint8_t* smem = smem_raw + pad + (kHq ? kHqBytes : 0);
+    const uint32_t tiles_addr = raw_addr + pad + (kHq ? kHqBytes : 0);
     float4* xch = reinterpret_cast<float4*>(smem + size_t(kStages) * kStageBytes);  // [2][kBM]
     uint64_t* bars = reinterpret_cast<uint64_t*>(xch + 2 * kBM);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBarriers);
@@ -140,8 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto pfull_bar = [&](int b) { return smem_u32(bars + 2 * kStages + b); };
     auto pempty_bar = [&](int b) { return smem_u32(bars + 2 * kStages + kPartBufs + b); };
     const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 2 * kPartBufs);
+    const uint32_t hq_bar = drain_bar + 8;  // kHq: h codes and scales written
     auto a_tile = [&](int s) { return tiles_addr + uint32_t(s) * kStageBytes; };
-    auto b_tile = [&](int s) { return a_tile(s) + kAMaxBytes; };
+    auto b_tile = [&](int s) { return a_tile(s) + (kHq ? 0u : uint32_t(kAMaxBytes)); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -156,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(pempty_bar(b), kEpiWarps);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(hq_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -180,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
-            const uint32_t bytes = uint32_t(p.a_rows) * 128u + kKbBytesW;
+            const uint32_t bytes = (kHq ? 0u : uint32_t(p.a_rows) * 128u) + kKbBytesW;
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 int m, n;
                 tile_coords(p, tile, m, n);
@@ -190,7 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full_bar(stage), bytes);
-                    tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage), kb * 128, m * kBM);
+                    if constexpr (!kHq)
+                        tma_load_2d(&tmap_h, full_bar(stage), a_tile(stage), kb * 128, m * kBM);
                     tma_load_2d(&tmap_w, full_bar(stage), b_tile(stage), 0,
                                 (n * p.num_kb + kb) * kBN);
                     ++issued;
@@ -212,6 +308,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
             bool ok = true;
+            if constexpr (kHq) {  // the h codes, written by the epilogue warps, come first
+                ok = wait_bounded(hq_bar, 0, abort_flag);
+                tc_fence_after_sync();
+            }
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bounded(pempty_bar(buf), buf_phase ^ 1u, abort_flag) ||
@@ -221,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after_sync();
                     const uint32_t d_tmem = tmem_base + buf * uint32_t(kBN);
-                    const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage));
+                    const uint64_t a_desc = sw128_kmajor_desc(
+                        kHq ? hq_addr + uint32_t(kb) * uint32_t(kHqRows * 128) : a_tile(stage));
                     const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage));
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {  // 32 codes = 32 bytes of every row each
@@ -255,23 +356,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t buf = 0, buf_phase = 0;
         int par = 0;  // exchange buffer of this tile
         bool ok = true;
+        if constexpr (kHq) {
+            quantise_h_blocks(p.h, int(p.T), p.num_kb * 128, warp - 2, lane, hq, hq_scale);
+            fence_proxy_async_shared();  // the codes are read by the tensor core
+            asm volatile("bar.sync 5, %0;" ::"n"(kEpiWarps * 32) : "memory");
+            if (warp == 2 && lane == 0) mbar_arrive(hq_bar);
+        }
         for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
             int m, n;
             tile_coords(p, tile, m, n);
             const int64_t row = int64_t(m) * kBM + row_in_tile;
             const bool live = row < p.T;
             const int wblk = 2 * n + half;  // this half's 128-row weight block
-            const float* shr = p.sh + (live ? row : 0) * p.num_kb;
+            const float* shr = kHq ? hq_scale + (live ? row : 0) * p.num_kb
+                                   : p.sh + (live ? row : 0) * p.num_kb;
             const float* swr = p.sw + int64_t(wblk < nvb ? wblk : 0) * p.num_kb;
             float acc[kHalfN];
 #pragma unroll
             for (int j = 0; j < kHalfN; ++j) acc[j] = 0.0f;
-            float s_next = (live && wblk < nvb) ? __fmul_rn(__ldg(shr), __ldg(swr)) : 0.0f;
+            float s_next = (live && wblk < nvb) ? __fmul_rn(kHq ? shr[0] : __ldg(shr), __ldg(swr)) : 0.0f;
             for (int kb = 0; kb < p.num_kb; ++kb) {
                 const float s = s_next;
                 if (kb + 1 < p.num_kb)
-                    s_next = (live && wblk < nvb) ? __fmul_rn(__ldg(shr + kb + 1), __ldg(swr + kb + 1))
-                                                  : 0.0f;
+                    s_next = (live && wblk < nvb)
+                                 ? __fmul_rn(kHq ? shr[kb + 1] : __ldg(shr + kb + 1), __ldg(swr + kb + 1))
+                                 : 0.0f;
                 int got = 1;
                 if (lane == 0) got = wait_bounded(pfull_bar(buf), buf_phase, abort_flag) ? 1 : 0;
                 got = __shfl_sync(0xffffffffu, got, 0);
@@ -355,25 +464,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-int g_configured[64];
+int g_configured[2][64];  // per variant (kHq) and device
 
-}  // namespace
-
-cudaError_t launch_lmhead_partials_fp8_block(const CUtensorMap* th, const CUtensorMap* tw,
-                                             const int32_t* targets, const float* sh,
-                                             const float* sw, void* partials, int64_t T,
-                                             int64_t V, int64_t H, float inv_temp, int num_sms,
-                                             cudaStream_t stream) {
+template <bool kHq>
+cudaError_t launch_fp8b(const CUtensorMap* th, const CUtensorMap* tw, const Args& a, int num_sms,
+                        cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!g_configured[dev]) {
-        e = cudaFuncSetAttribute(lmhead_fp8b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(kSmemBytes));
+    auto kernel = lmhead_fp8b_kernel<kHq>;
+    if (!g_configured[kHq ? 1 : 0][dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem_bytes<kHq>()));
         if (e != cudaSuccess) return e;
-        g_configured[dev] = 1;
+        g_configured[kHq ? 1 : 0][dev] = 1;
     }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(a.num_tiles < num_sms ? a.num_tiles : num_sms, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<kHq>();
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, *th, *tw, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+Args fp8b_args(const int32_t* targets, const float* sh, const float* sw, void* partials,
+               int64_t T, int64_t V, int64_t H, float inv_temp) {
     Args a = {};
     a.targets = targets;
     a.partials = static_cast<float4*>(partials);
@@ -388,19 +511,31 @@ cudaError_t launch_lmhead_partials_fp8_block(const CUtensorMap* th, const CUtens
     a.band = a.num_m < 32 ? a.num_m : 32;
     a.num_tiles = a.num_m * a.num_n;
     a.inv_temp = inv_temp;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(a.num_tiles < num_sms ? a.num_tiles : num_sms, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, lmhead_fp8b_kernel, *th, *tw, a);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return a;
+}
+
+}  // namespace
+
+cudaError_t launch_lmhead_partials_fp8_block(const CUtensorMap* th, const CUtensorMap* tw,
+                                             const int32_t* targets, const float* sh,
+                                             const float* sw, void* partials, int64_t T,
+                                             int64_t V, int64_t H, float inv_temp, int num_sms,
+                                             cudaStream_t stream) {
+    return launch_fp8b<false>(th, tw, fp8b_args(targets, sh, sw, partials, T, V, H, inv_temp),
+                              num_sms, stream);
+}
+
+bool lmhead_fp8b_quantises_h(int64_t T, int64_t H) {
+    return T >= 1 && T <= kHqMaxRows && H <= kHqMaxH && H % 128 == 0;
+}
+
+cudaError_t launch_lmhead_partials_fp8_block_hq(const CUtensorMap* tw, const void* h_bf16,
+                                                const int32_t* targets, const float* sw,
+                                                void* partials, int64_t T, int64_t V, int64_t H,
+                                                float inv_temp, int num_sms, cudaStream_t stream) {
+    Args a = fp8b_args(targets, nullptr, sw, partials, T, V, H, inv_temp);
+    a.h = static_cast<const __nv_bfloat16*>(h_bf16);
+    return launch_fp8b<true>(tw, tw, a, num_sms, stream);  // no h tensor map: tw stands in
 }
 
 int lmhead_fp8b_a_box_rows(int64_t T) {

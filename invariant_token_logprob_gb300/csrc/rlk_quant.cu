@@ -216,14 +216,23 @@ __global__ void __launch_bounds__(kQuantThreads)
     const int64_t r = int64_t(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
     if (r >= out_rows) return;  // uniform per warp
     const int nkb = H / 128;
-    for (int k = lane * 16; k < H; k += 32 * 16) {  // H % 128 == 0: whole blocks per step
-        if (r >= rows) {
-            *reinterpret_cast<uint4*>(codes + r * int64_t(H) + k) = make_uint4(0u, 0u, 0u, 0u);
+    // every lane runs every step (H % 128 == 0: whole blocks of 8 lanes); the
+    // lanes past the row end compute on zeros and store nothing, so the
+    // shuffles below see the whole warp
+    for (int k0 = 0; k0 < H; k0 += 32 * 16) {
+        const int k = k0 + lane * 16;
+        const bool act = k < H;
+        if (r >= rows) {  // zero padding rows (uniform per warp: no shuffle)
+            if (act)
+                *reinterpret_cast<uint4*>(codes + r * int64_t(H) + k) = make_uint4(0u, 0u, 0u, 0u);
             continue;
         }
-        const __nv_bfloat16* xr = x + r * int64_t(H) + k;
-        const uint4 v0 = *reinterpret_cast<const uint4*>(xr);
-        const uint4 v1 = *reinterpret_cast<const uint4*>(xr + 8);
+        uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+        if (act) {
+            const __nv_bfloat16* xr = x + r * int64_t(H) + k;
+            v0 = *reinterpret_cast<const uint4*>(xr);
+            v1 = *reinterpret_cast<const uint4*>(xr + 8);
+        }
         float amax = 0.0f;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -238,6 +247,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
         for (int off = 4; off >= 1; off >>= 1)  // the 8 lanes of this 128-element block
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (!act) continue;
         const float sc = e4m3_scale(amax);
         const bool fast = sc >= kE4m3FastScaleMin;
         const float rs = fast ? __frcp_rn(sc) : 0.0f;
