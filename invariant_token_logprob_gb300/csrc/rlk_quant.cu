@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 // warp shuffle; then the conversion of quantize_rows_kernel from the registers
 // (same scale, same division, same conversion: bit-identical codes and
 // scales).  Three CTAs of 8 warps per SM (80 registers) keep 192 KB of W in
-// flight per SM.  At V = 151936, H = 4096 (one box, CUDA events): 272 us for
+// flight per SM.  At V = 151936, H = 4096 (one GB300, CUDA events): 272 us for
 // 1.87 GB, against 308 us for a warp-per-row kernel staging each row in shared
 // memory by one bulk copy (28 warps per SM), and 311 us at four CTAs per SM
 // (spills).  Rows past `rows` (padding of the last vocabulary tile) get zero
@@ -310,7 +310,7 @@ __device__ __forceinline__ uint32_t e4m3x4_paired(float a, float b, float c, flo
 // 256-byte row pieces and every warp-wide store writes 2 x 128 contiguous code
 // bytes.  The block's max meets through warp shuffles and shared memory; the
 // codes come from e4m3x4_paired.  Three CTAs per SM (at most 80 registers a
-// thread, no spills).  At V = 151936, H = 4096 (one box, CUDA events): 289 us
+// thread, no spills).  At V = 151936, H = 4096 (one GB300, CUDA events): 289 us
 // = 0.95 of the measured HBM copy bandwidth for 1.87 GB, against 386 us when a
 // thread pair held one row's 128 elements (16 rows per warp-wide load), 320 us
 // for this mapping with scalar arithmetic, 368 us with paired arithmetic at
