@@ -27,6 +27,11 @@
 //               block reduces its half to a (m, s, a, zt) record.  The two
 //               halves of a row meet through shared memory (half 0 then half 1,
 //               the combine of the merge), one 16-byte record per row and tile.
+// Calls of at most 4 rows (H <= 4096) take the kHq variant: the epilogue
+// warps first quantise the bf16 h rows themselves (the block quantiser's
+// arithmetic, so the same codes and scales) into a resident 16-row block in
+// front of the stages, the MMA reads h from there, and the ring carries W
+// only; a decode step then needs no quantiser launch before this kernel.
 // A row's bits depend only on its own codes and scales and the fixed k-block
 // order: the tile shape is fixed and rows never mix.  There is one launch
 // shape for every T.  Every wait is bounded in time (2 s); on expiry the
