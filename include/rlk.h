@@ -277,7 +277,7 @@ rlk_status rlk_logprob_fp8(const void *hidden_bf16, const uint8_t *weight_e4m3,
  *   scales [ceil(V/128)][H/128] f32 (rlk_fp8_block_weight_scale_count(V, H)
  *   floats).  Asynchronous; run once per weight update.
  * rlk_logprob_fp8_block: quantise h into the workspace, then the block-FP8
- *   LM-head kernel and the fixed-tree merge.  Calls of at most 4 rows with
+ *   LM-head kernel and the fixed-tree merge.  Calls of at most 16 rows with
  *   H <= 4096 quantise h inside the LM-head kernel instead (the same codes
  *   and scales, so the same bits).  weight_e4m3 / weight_scales_f32
  *   as produced by rlk_quantize_fp8_weight_blocks; workspace >=

@@ -151,7 +151,7 @@ cudaError_t launch_lmhead_partials_fp8_block(const CUtensorMap* th, const CUtens
                                              const float* sw, void* partials, int64_t T,
                                              int64_t V, int64_t H, float inv_temp, int num_sms,
                                              cudaStream_t stream);
-// Calls of at most 4 rows with H <= 4096 (H % 128 == 0) quantise h in the
+// Calls of at most 16 rows with H <= 4096 (H % 128 == 0) quantise h in the
 // block-FP8 kernel: the bf16 h rows are read directly (no quantiser launch,
 // no h tensor map; tw as above), with the block quantiser's codes and scales.
 bool lmhead_fp8b_quantises_h(int64_t T, int64_t H);

@@ -27,7 +27,7 @@
 //               block reduces its half to a (m, s, a, zt) record.  The two
 //               halves of a row meet through shared memory (half 0 then half 1,
 //               the combine of the merge), one 16-byte record per row and tile.
-// Calls of at most 4 rows (H <= 4096) take the kHq variant: the epilogue
+// Calls of at most 16 rows (H <= 4096) take the kHq variant: the epilogue
 // warps first quantise the bf16 h rows themselves (the block quantiser's
 // arithmetic, so the same codes and scales) into a resident 16-row block in
 // front of the stages, the MMA reads h from there, and the ring carries W
@@ -57,12 +57,12 @@ constexpr int kStages = 4;
 // quantise h into a resident block of kHqRows rows in front of the stages,
 // with its block scales; the ring then carries W only.
 constexpr int kHqRows = kMinTmaRows;  // 16: the rows of the resident block
-constexpr int kHqMaxRows = 4;
+constexpr int kHqMaxRows = kHqRows;
 constexpr int kHqMaxH = 4096;
-constexpr int kHqCodeBytes = kHqRows * kHqMaxH;              // 64 KB
-constexpr int kHqScaleBytes = kHqMaxRows * (kHqMaxH / 128) * 4;  // 512 B
-constexpr int kHqBytes = kHqCodeBytes + 1024;                  // codes + scales, 1 KB aligned
-static_assert(kHqScaleBytes <= 1024, "h block scales fit their slot");
+constexpr int kHqCodeBytes = kHqRows * kHqMaxH;                  // 64 KB
+constexpr int kHqScaleBytes = kHqMaxRows * (kHqMaxH / 128) * 4;  // 2 KB
+constexpr int kHqBytes = kHqCodeBytes + kHqScaleBytes;           // 1 KB aligned
+static_assert(kHqBytes % 1024 == 0, "stages after the h block stay 1 KB aligned");
 template <bool kHq>
 constexpr int stage_bytes() { return (kHq ? 0 : kAMaxBytes) + kKbBytesW; }
 constexpr int kPartBufs = 2;
@@ -142,69 +142,93 @@ __device__ __forceinline__ void pair_warps_sync(int q) {
     asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
 }
 
-// kHq: two warps per row (at most kHqMaxRows rows), each taking half of the
-// row's 128-element blocks, lane l 16 consecutive elements per step of four
-// blocks; every lane runs every step (the lanes of a block past the half
-// compute on zeros and store nothing), so the shuffles see the whole warp.
-// The block max meets over the block's 8 lanes; then the scale and codes of
-// the block quantiser kernel (same arithmetic, same bits), written at the
-// row's place in the resident 128-byte-swizzled block (16 codes = one 16-byte
-// chunk) and the scale at [row][block].
+// kHq: the work items are (row, half of the row's 128-element blocks), item
+// i = 2 r + half for r < T; epilogue warp w takes items w, w + 8, ..., two at
+// a time with all their loads issued first.  Lane l takes 16 consecutive
+// elements per step of four blocks (at most kHqSteps steps per item); every
+// lane runs every step (the lanes of a block past the item's end compute on
+// zeros and store nothing), so the shuffles see the whole warp.  The block max
+// meets over the block's 8 lanes; then the scale and codes of the block
+// quantiser kernel (same arithmetic, same bits), written at the row's place in
+// the resident 128-byte-swizzled block (16 codes = one 16-byte chunk) and the
+// scale at [row][block].
+constexpr int kHqSteps = kHqMaxH / 2 / 512;  // steps of 512 elements per half row
+constexpr int kHqItemsPerRound = 2;
+
 __device__ __forceinline__ void quantise_h_blocks(const __nv_bfloat16* __restrict__ h, int T,
                                                   int H, int w, int lane, uint8_t* hq,
                                                   float* hq_scale) {
-    const int r = w >> 1;
-    if (r >= T) return;  // whole warps
     const int nkb = H / 128;
     const int kb_mid = (nkb + 1) / 2;
-    const int k_begin = (w & 1) ? kb_mid * 128 : 0;
-    const int k_end = (w & 1) ? nkb * 128 : kb_mid * 128;
-    for (int k0 = k_begin; k0 < k_end; k0 += 32 * 16) {
-        const int k = k0 + lane * 16;
-        const bool act = k < k_end;
-        uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-        if (act) {
-            const __nv_bfloat16* xr = h + int64_t(r) * H + k;
-            v0 = __ldg(reinterpret_cast<const uint4*>(xr));
-            v1 = __ldg(reinterpret_cast<const uint4*>(xr + 8));
-        }
-        float amax = 0.0f;
+    for (int it0 = w; it0 < 2 * T; it0 += kEpiWarps * kHqItemsPerRound) {
+        uint4 v[kHqItemsPerRound][kHqSteps][2];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(hh ? &v1 : &v0);
+        for (int j = 0; j < kHqItemsPerRound; ++j) {
+            const int it = it0 + j * kEpiWarps;
+            const int r = it >> 1;
+            const int k_begin = (it & 1) ? kb_mid * 128 : 0;
+            const int k_end = (it & 1) ? nkb * 128 : kb_mid * 128;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 f = __bfloat1622float2(p2[i]);
-                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            for (int st = 0; st < kHqSteps; ++st) {
+                const int k = k_begin + st * 512 + lane * 16;
+                v[j][st][0] = v[j][st][1] = make_uint4(0u, 0u, 0u, 0u);
+                if (it < 2 * T && k < k_end) {
+                    const __nv_bfloat16* xr = h + int64_t(r) * H + k;
+                    v[j][st][0] = __ldg(reinterpret_cast<const uint4*>(xr));
+                    v[j][st][1] = __ldg(reinterpret_cast<const uint4*>(xr + 8));
+                }
             }
         }
 #pragma unroll
-        for (int off = 4; off >= 1; off >>= 1)  // the 8 lanes of this 128-element block
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        if (!act) continue;
-        const float sc = e4m3_scale(amax);
-        const bool fast = sc >= kE4m3FastScaleMin;
-        const float rs = fast ? __frcp_rn(sc) : 0.0f;
-        uint32_t out[4];
+        for (int j = 0; j < kHqItemsPerRound; ++j) {
+            const int it = it0 + j * kEpiWarps;
+            if (it >= 2 * T) break;  // whole warps
+            const int r = it >> 1;
+            const int k_begin = (it & 1) ? kb_mid * 128 : 0;
+            const int k_end = (it & 1) ? nkb * 128 : kb_mid * 128;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(hh ? &v1 : &v0);
-            const float2 a = __bfloat1622float2(p2[0]), b = __bfloat1622float2(p2[1]);
-            const float2 c = __bfloat1622float2(p2[2]), d = __bfloat1622float2(p2[3]);
-            if (fast) {
-                out[2 * hh] = e4m3x4<true>(a.x, a.y, b.x, b.y, sc, rs);
-                out[2 * hh + 1] = e4m3x4<true>(c.x, c.y, d.x, d.y, sc, rs);
-            } else {
-                out[2 * hh] = e4m3x4<false>(a.x, a.y, b.x, b.y, sc, rs);
-                out[2 * hh + 1] = e4m3x4<false>(c.x, c.y, d.x, d.y, sc, rs);
+            for (int st = 0; st < kHqSteps; ++st) {
+                const int k = k_begin + st * 512 + lane * 16;
+                const bool act = k < k_end;
+                float amax = 0.0f;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v[j][st][hh]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = __bfloat1622float2(p2[i]);
+                        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+                    }
+                }
+#pragma unroll
+                for (int off = 4; off >= 1; off >>= 1)  // the 8 lanes of this 128-element block
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                if (!act) continue;
+                const float sc = e4m3_scale(amax);
+                const bool fast = sc >= kE4m3FastScaleMin;
+                const float rs = fast ? __frcp_rn(sc) : 0.0f;
+                uint32_t out[4];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v[j][st][hh]);
+                    const float2 a = __bfloat1622float2(p2[0]), b = __bfloat1622float2(p2[1]);
+                    const float2 c = __bfloat1622float2(p2[2]), d = __bfloat1622float2(p2[3]);
+                    if (fast) {
+                        out[2 * hh] = e4m3x4<true>(a.x, a.y, b.x, b.y, sc, rs);
+                        out[2 * hh + 1] = e4m3x4<true>(c.x, c.y, d.x, d.y, sc, rs);
+                    } else {
+                        out[2 * hh] = e4m3x4<false>(a.x, a.y, b.x, b.y, sc, rs);
+                        out[2 * hh + 1] = e4m3x4<false>(c.x, c.y, d.x, d.y, sc, rs);
+                    }
+                }
+                const int kb = k >> 7;
+                const int chunk = (k & 127) >> 4;
+                *reinterpret_cast<uint4*>(hq + kb * (kHqRows * 128) + (r >> 3) * 1024 +
+                                          (r & 7) * 128 + ((chunk ^ (r & 7)) << 4)) =
+                    make_uint4(out[0], out[1], out[2], out[3]);
+                if ((lane & 7) == 0) hq_scale[r * nkb + kb] = sc;
             }
         }
-        const int kb = k >> 7;
-        const int chunk = (k & 127) >> 4;
-        *reinterpret_cast<uint4*>(hq + kb * (kHqRows * 128) + (r >> 3) * 1024 + (r & 7) * 128 +
-                                  ((chunk ^ (r & 7)) << 4)) =
-            make_uint4(out[0], out[1], out[2], out[3]);
-        if ((lane & 7) == 0) hq_scale[r * nkb + kb] = sc;
     }
 }
 

@@ -129,14 +129,14 @@ def test_block_fp8_logprob_matches_oracle(olib, T, H, V, it):
 
 @pytest.mark.parametrize("H", [128, 384, 4096])
 def test_block_fp8_decode_quantises_h_in_the_kernel(olib, H):
-    """Calls of at most 4 rows quantise h in the block-FP8 kernel (1 x 128
-    blocks, two warps per row).  Their rows must carry the bits of an 8-row
-    call, which runs the block quantiser kernel, and match the oracle on the
-    GPU quantiser's codes.  H = 128 is one k block (one warp per row idle),
-    H = 384 an odd number of blocks.  A zero row and a tiny row check the
-    scale-1 and subnormal paths."""
+    """Calls of at most 16 rows quantise h in the block-FP8 kernel (1 x 128
+    blocks, two work items per row).  Their rows must carry the bits of a
+    32-row call, which runs the block quantiser kernel, and match the oracle
+    on the GPU quantiser's codes.  H = 128 is one k block (the second half of
+    each row empty), H = 384 an odd number of blocks.  A zero row and a tiny
+    row check the scale-1 and subnormal paths."""
     import invariant_token_logprob_gb300 as rlk
-    T, V = 8, 1000
+    T, V = 32, 1000
     d = to_dev(lm_head_inputs(T, H, V, seed=H + 5, hidden="normal", w_std=0.05))
     d["h"][2] = 0.0
     d["h"][3] = (d["h"][3].float() * 1e-30).to(torch.bfloat16)
@@ -145,7 +145,7 @@ def test_block_fp8_decode_quantises_h_in_the_kernel(olib, H):
     rlk.check_device_error()
     ref = oracle.logprob_fp8_block(hc, hs, wc, ws_, d["targets"].cpu(), 1.0, lib=olib)
     assert_parity(full, ref, what=f"block fp8 H={H}")
-    for c in (1, 2, 3, 4):
+    for c in (1, 2, 3, 4, 5, 8, 15, 16):
         parts = [_np(rlk.logprob_fp8_block(d["h"][i:i + c].contiguous(), wp, ws,
                                            d["targets"][i:i + c].contiguous(), V))
                  for i in range(0, T, c)]
